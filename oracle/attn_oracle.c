@@ -1,0 +1,173 @@
+/*
+ * Exact self-attention forward in fp64 on the CPU: the ORACLE.
+ *
+ * This file is test infrastructure. Only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg load it; the CUDA path never does, and the two
+ * share no code, header or table.
+ *
+ * What it computes is the plain attention graph of "From Attention Graph to
+ * FlashAttention - A Memory-Centric Compilation Approach in AICF", section 1
+ * (Introduction): Scores = Q x K^T, Scores = Mask(Scores), Scores =
+ * Softmax(Scores), Output = Scores x V.  The streaming pass that the CUDA path
+ * runs is, per section 3 of the same page, a new execution structure for that
+ * same operation, not a new operation, so its result must equal this one up to
+ * rounding.  The AttenIO abstract ("I/O Analysis is All You Need", ASPLOS 2026)
+ * calls the target "exact" long-sequence self-attention for the same reason.
+ *
+ * Readings where the pages are silent (each one is also listed in the design
+ * notes):
+ *   - scores are multiplied by `scale` before the mask and the softmax;
+ *   - the causal mask keeps key j for query i iff j <= i, and a masked score
+ *     is -infinity (it drops out of the softmax sum);
+ *   - LSE_i = ln sum_j exp(scale * q_i . k_j) over the kept keys, i.e. the
+ *     natural-log normaliser of the softmax, including the scale;
+ *   - Q, K, V are the bf16-rounded inputs, decoded exactly to double.
+ *
+ * Layout: Q, K, V are [BH, N, d] arrays of bf16 bit patterns (uint16), d
+ * fastest.  Outputs are double.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* bf16 -> double, exactly: a bf16 value is the top half of an IEEE float. */
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * One query row of one (batch, head): the four steps of the attention graph.
+ *   q   : [d] query row (bf16 bits)
+ *   Kh  : [N, d] keys of this head, Vh : [N, d] values of this head
+ *   i   : the query's position (used only by the causal mask)
+ *   s   : [N] scratch for the scores; on return it holds the probabilities
+ *   o   : [d] output row, *lse : log-sum-exp of the scaled, masked scores
+ */
+static void attend_one_row(const uint16_t *q, const uint16_t *Kh, const uint16_t *Vh,
+                           int64_t N, int64_t d, int64_t i, int causal, double scale,
+                           double *s, double *o, double *lse)
+{
+    /* Scores = Q x K^T (times the scale). */
+    for (int64_t j = 0; j < N; ++j) {
+        const uint16_t *kj = Kh + j * d;
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            acc += bf16_bits_to_double(q[c]) * bf16_bits_to_double(kj[c]);
+        s[j] = scale * acc;
+    }
+    /* Scores = Mask(Scores): keys after the query are removed. */
+    if (causal)
+        for (int64_t j = i + 1; j < N; ++j)
+            s[j] = -INFINITY;
+    /* Scores = Softmax(Scores), with the row maximum taken out first so that
+     * exp() cannot overflow; the maximum cancels in the ratio. */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < N; ++j)
+        if (s[j] > m) m = s[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        s[j] = exp(s[j] - m); /* exp(-inf) = 0 for masked keys */
+        l += s[j];
+    }
+    for (int64_t j = 0; j < N; ++j)
+        s[j] /= l;
+    /* Output = Scores x V. */
+    for (int64_t c = 0; c < d; ++c)
+        o[c] = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        if (s[j] == 0.0) continue;
+        const uint16_t *vj = Vh + j * d;
+        for (int64_t c = 0; c < d; ++c)
+            o[c] += s[j] * bf16_bits_to_double(vj[c]);
+    }
+    *lse = m + log(l);
+}
+
+typedef struct {
+    const uint16_t *Q, *K, *V;
+    int64_t BH, N, d, R;
+    int causal;
+    double scale;
+    const int64_t *rows; /* [BH, R] query positions, or NULL for all rows */
+    double *O;           /* [BH, R, d] */
+    double *LSE;         /* [BH, R] */
+    double *P;           /* [BH, R, N] probabilities, or NULL */
+    int64_t first, last; /* work items [first, last) of BH*R */
+    int status;
+} oracle_job;
+
+static void *oracle_worker(void *arg)
+{
+    oracle_job *job = (oracle_job *)arg;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(job->N > 0 ? job->N : 1));
+    if (!s) { job->status = 2; return NULL; }
+    for (int64_t w = job->first; w < job->last; ++w) {
+        int64_t bh = w / job->R, r = w % job->R;
+        int64_t i = job->rows ? job->rows[w] : r;
+        if (i < 0 || i >= job->N) { job->status = 1; break; }
+        const int64_t head = bh * job->N * job->d;
+        attend_one_row(job->Q + head + i * job->d, job->K + head, job->V + head,
+                       job->N, job->d, i, job->causal, job->scale, s,
+                       job->O + w * job->d, job->LSE + w);
+        if (job->P)
+            memcpy(job->P + w * job->N, s, sizeof(double) * (size_t)job->N);
+    }
+    free(s);
+    return NULL;
+}
+
+/*
+ * Attention forward for selected query rows, fp64, threaded over rows.
+ *   Q, K, V   : [BH, N, d] bf16 bit patterns
+ *   rows      : [BH, R] query positions per (batch, head), or NULL meaning
+ *               R == N and every row in order
+ *   O, LSE, P : outputs as above (P may be NULL)
+ *   nthreads  : worker threads (>= 1)
+ * Returns 0, or 1 for a bad argument / row index, 2 for out of memory.
+ */
+int oracle_attn_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                     int64_t BH, int64_t N, int64_t d, int causal, double scale,
+                     const int64_t *rows, int64_t R,
+                     double *O, double *LSE, double *P, int nthreads)
+{
+    if (!Q || !K || !V || !O || !LSE || BH < 0 || N < 1 || d < 1 || R < 0)
+        return 1;
+    if (!rows && R != N)
+        return 1;
+    const int64_t items = BH * R;
+    if (items == 0)
+        return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > items) nthreads = (int)items;
+    oracle_job *jobs = (oracle_job *)calloc((size_t)nthreads, sizeof(oracle_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(jobs); free(tids); return 2; }
+    for (int t = 0; t < nthreads; ++t) {
+        oracle_job j = {Q, K, V, BH, N, d, R, causal, scale, rows, O, LSE, P,
+                        items * t / nthreads, items * (t + 1) / nthreads, 0};
+        jobs[t] = j;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, oracle_worker, &jobs[t]) != 0) break;
+        started = t;
+    }
+    oracle_worker(&jobs[0]);
+    /* Threads that failed to start: run their share here. */
+    for (int t = started + 1; t < nthreads; ++t)
+        oracle_worker(&jobs[t]);
+    int status = jobs[0].status;
+    for (int t = 1; t <= started; ++t)
+        pthread_join(tids[t], NULL);
+    for (int t = 1; t < nthreads; ++t)
+        if (jobs[t].status) status = jobs[t].status;
+    free(jobs);
+    free(tids);
+    return status;
+}

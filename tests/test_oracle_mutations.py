@@ -1,0 +1,75 @@
+"""Planted mistakes: every plausible slip in the oracle must fail at least one pin.
+
+Each case copies the oracle's C source, applies one textual mutation (a dropped
+term, an off-by-one mask, a wrong index, ...), compiles the copy on the CPU and
+runs the pins of ``test_oracle.py`` against it. A mutant that passes every pin
+would mean the pins could not tell that mistake from the definition.
+"""
+import inspect
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+
+MUTATIONS = {
+    "mask_keeps_diagonal_out": ("for (int64_t j = i + 1; j < N; ++j)", "for (int64_t j = i; j < N; ++j)"),
+    "mask_lets_next_key_in": ("for (int64_t j = i + 1; j < N; ++j)", "for (int64_t j = i + 2; j < N; ++j)"),
+    "scale_dropped": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),
+    "lse_log2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
+    "no_normalisation": ("s[j] /= l;", "s[j] /= (l > 1.0 ? 1.0 : 1.0);"),
+    "value_row_of_query": ("const uint16_t *vj = Vh + j * d;", "const uint16_t *vj = Vh + i * d;"),
+    "key_row_of_query": ("const uint16_t *kj = Kh + j * d;", "const uint16_t *kj = Kh + i * d;"),
+    "no_max_subtraction": ("s[j] = exp(s[j] - m);", "s[j] = exp(s[j]);"),
+    "head_offset_dropped_for_kv": ("job->Q + head + i * job->d, job->K + head, job->V + head,",
+                                   "job->Q + head + i * job->d, job->K, job->V,"),
+    "bf16_decoded_as_low_half": ("uint32_t u = ((uint32_t)bits) << 16;", "uint32_t u = ((uint32_t)bits) << 15;"),
+    "max_ignores_first_key": ("for (int64_t j = 0; j < N; ++j)\n        if (s[j] > m) m = s[j];",
+                              "for (int64_t j = 1; j < N; ++j)\n        if (s[j] > m) m = s[j];"),
+}
+
+
+def _pin_functions():
+    out = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_") or "oracle_mod" not in inspect.signature(fn).parameters:
+            continue
+        marks = getattr(fn, "pytestmark", [])
+        grid = [{}]
+        for m in marks:
+            if m.name == "parametrize":
+                names = [n.strip() for n in m.args[0].split(",")] if isinstance(m.args[0], str) else m.args[0]
+                new = []
+                for g in grid:
+                    for val in m.args[1]:
+                        vals = val if len(names) > 1 else (val,)
+                        new.append({**g, **dict(zip(names, vals))})
+                grid = new
+        for kw in grid:
+            out.append((name, fn, kw))
+    return out
+
+
+@pytest.mark.parametrize("mutation", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(tmp_path, mutation):
+    old, new = MUTATIONS[mutation]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found exactly once: {old!r}"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    str(mutant_c), "-o", str(lib), "-lm"], check=True)
+    mutant = oracle.OracleBuild(str(lib))
+    caught = []
+    for name, fn, kw in _pin_functions():
+        try:
+            fn(mutant, **kw)
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(name)
+    assert caught, f"no pin caught mutation {mutation}"
