@@ -1,1 +1,202 @@
-"""GB300-native exact self-attention forward (placeholder; binding follows)."""
+"""GB300 (sm_103a) exact self-attention forward: Python binding of the C ABI.
+
+This module only marshals arguments: every step of the computation runs in the
+CUDA kernels of ``libexact_attn.so`` (see ``include/exact_attn.h``). PyTorch is
+used for device memory and streams. There is no fallback: if the library is
+not built, or no sm_103 GPU is present, the calls raise.
+
+    import exact_long_sequence_gb300 as ela
+    o, lse = ela.attn_fwd(q, k, v, causal=True)   # q, k, v: bf16 [B, H, N, d] on cuda
+
+The operation is O = softmax(scale * Q K^T + mask) V with the per-row natural
+log-sum-exp LSE, computed as the streaming tiled pass of "From Attention Graph
+to FlashAttention - A Memory-Centric Compilation Approach in AICF", section 3.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import workloads  # noqa: F401  (seeded synthetic inputs; no attention arithmetic)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libexact_attn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_MISALIGNED = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_TIMEOUT = 5
+ATTN_ERR_NO_DEVICE = 6
+
+# Every symbol include/exact_attn.h declares.
+EXPORTED_SYMBOLS = (
+    "attn_fwd",
+    "attn_fwd_host",
+    "attn_fwd_host_workspace_bytes",
+    "attn_plan",
+    "attn_last_device_error",
+    "attn_last_cuda_error",
+    "attn_strerror",
+    "attn_debug_wait_timeout",
+)
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str, lib=None):
+        msg = f"{what}: status {status}"
+        if lib is not None:
+            msg += f" ({lib.attn_strerror(status).decode()})"
+            if status == ATTN_ERR_CUDA:
+                msg += f", cudaError {lib.attn_last_cuda_error()}"
+        super().__init__(msg)
+        self.status = status
+
+
+class AttnPlan(ctypes.Structure):
+    _fields_ = [
+        ("Br", ctypes.c_int), ("Bc", ctypes.c_int), ("q_tiles", ctypes.c_int), ("kv_stages", ctypes.c_int),
+        ("tmem_cols", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int),
+        ("num_units", ctypes.c_int), ("grid", ctypes.c_int), ("heads_per_group", ctypes.c_int),
+        ("flops", ctypes.c_double), ("io_bytes", ctypes.c_double), ("l2_bytes", ctypes.c_double),
+        ("hbm_bytes", ctypes.c_double), ("io_opt_q_tiles", ctypes.c_int), ("io_opt_Bc", ctypes.c_int),
+        ("io_opt_l2_bytes", ctypes.c_double),
+    ]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load the CUDA library (built by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+    lib.attn_fwd_host.restype = i
+    lib.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i]
+    lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(AttnPlan)]
+    lib.attn_plan.restype = i
+    lib.attn_last_device_error.argtypes = [vp]
+    lib.attn_last_device_error.restype = i
+    lib.attn_last_cuda_error.argtypes = []
+    lib.attn_last_cuda_error.restype = i
+    lib.attn_strerror.argtypes = [i]
+    lib.attn_strerror.restype = ctypes.c_char_p
+    lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.attn_debug_wait_timeout.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != ATTN_OK:
+        raise AttnError(status, what, _lib)
+
+
+def default_scale(d: int) -> float:
+    """1/sqrt(d), computed in double and rounded once to fp32."""
+    import torch
+
+    return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32).item())
+
+
+def _stream_handle(stream):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v) on the GPU through the C ABI.
+
+    q, k, v : bf16 CUDA tensors [B, H, N, d], contiguous, d in {64, 128}
+    out     : optional bf16 [B, H, N, d] output buffer; lse: optional fp32 [B, H, N]
+    stream  : torch.cuda.Stream (default: the current stream); the call is asynchronous.
+    """
+    import torch
+
+    lib = load_library()
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share a [B, H, N, d] shape")
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    with torch.cuda.device(q.device):
+        st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                          B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_host(q_h, k_h, v_h, causal: bool = False, scale: float | None = None, out_h=None, lse_h=None,
+                  workspace=None, stream=None):
+    """Same operation on HOST tensors (pin them for asynchronous copies): the library
+    copies Q, K, V in, runs the kernel and copies O, LSE out on `stream`. Synchronise the
+    stream before reading the outputs."""
+    import torch
+
+    lib = load_library()
+    B, H, N, d = q_h.shape
+    if scale is None:
+        scale = default_scale(d)
+    if out_h is None:
+        out_h = torch.empty_like(q_h, pin_memory=q_h.is_pinned())
+    if lse_h is None:
+        lse_h = torch.empty((B, H, N), dtype=torch.float32, pin_memory=q_h.is_pinned())
+    need = lib.attn_fwd_host_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = lib.attn_fwd_host(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(), out_h.data_ptr(), lse_h.data_ptr(),
+                           B, H, N, d, int(bool(causal)), float(scale), workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "attn_fwd_host")
+    return out_h, lse_h
+
+
+def host_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(load_library().attn_fwd_host_workspace_bytes(B, H, N, d))
+
+
+def attn_plan(B: int, H: int, N: int, d: int, causal: bool, num_sms: int = 0) -> dict:
+    """The planner's tiling for a shape (host only; num_sms=0 asks the current GPU)."""
+    lib = load_library()
+    plan = AttnPlan()
+    _check(lib.attn_plan(B, H, N, d, int(bool(causal)), num_sms, ctypes.byref(plan)), "attn_plan")
+    return plan.as_dict()
+
+
+def last_device_error(stream=None) -> int:
+    """Synchronise `stream` and return (and clear) the kernel error status."""
+    return load_library().attn_last_device_error(_stream_handle(stream))
+
+
+def debug_wait_timeout(timeout_ns: int, stream=None) -> int:
+    """Launch the bounded-wait test kernel (waits on a barrier nobody arrives on)."""
+    return load_library().attn_debug_wait_timeout(int(timeout_ns), _stream_handle(stream))

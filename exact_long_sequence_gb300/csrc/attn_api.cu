@@ -1,0 +1,263 @@
+// C ABI of the exact-attention forward: argument checks, tile plan, TMA
+// descriptors, the kernel launch, and the device error word.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/exact_attn.h"
+#include "attn_fwd_kernel.cuh"
+#include "plan.h"
+
+extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out);
+
+namespace elsattn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s for any single wait
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return ATTN_ERR_CUDA;
+}
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t* error_word = nullptr;  // 256-byte device block, first word = error code
+    bool smem_configured[2][2] = {{false, false}, {false, false}};
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver) return ATTN_ERR_NO_DEVICE;
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+        if ((e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if (s.cc_major != 10 || s.cc_minor != 3) return ATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        void* w = nullptr;
+        if ((e = cudaMalloc(&w, 256)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaMemset(w, 0, 256)) != cudaSuccess) {
+            cudaFree(w);
+            return cuda_fail(e);
+        }
+        s.error_word = static_cast<uint32_t*>(w);
+        s.ready = true;
+    }
+    *out = &s;
+    return ATTN_OK;
+}
+
+// Q, K, V viewed as a 3-D tensor [BH][N][d] (d innermost), read in boxes of
+// 64 columns x 128 rows with the 128-byte swizzle the tcgen05 descriptors
+// expect.  Rows past N read as zero.
+int encode_qkv_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBr), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_args(const void* Q, const void* K, const void* V, const void* O, const void* LSE, int B, int H, int N,
+               int d, float scale) {
+    if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H * N >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return ATTN_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return ATTN_ERR_MISALIGNED;
+    return ATTN_OK;
+}
+
+template <int D, bool CAUSAL>
+int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, const CUtensorMap& tk,
+           const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream) {
+    auto kernel = attn_fwd_kernel<D, CAUSAL>;
+    bool& configured = dev.smem_configured[D == 128][CAUSAL];
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem_bytes);
+        if (e != cudaSuccess) return cuda_fail(e);
+        configured = true;
+    }
+    kernel<<<plan.grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace elsattn
+
+using namespace elsattn;
+
+extern "C" int attn_plan(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out) {
+    if (!out) return ATTN_ERR_INVALID_ARG;
+    if (num_sms <= 0) {
+        DeviceState* dev = nullptr;
+        int st = device_state(&dev);
+        if (st != ATTN_OK) return st;
+        num_sms = dev->num_sms;
+    }
+    return attn_plan_impl(B, H, N, d, causal, num_sms, out);
+}
+
+extern "C" int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                        int d, int causal, float scale, cudaStream_t stream) {
+    int st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
+    if (st != ATTN_OK) return st;
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    attn_plan_t plan;
+    if ((st = attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan)) != ATTN_OK) return st;
+
+    const int BH = B * H;
+    CUtensorMap tq, tk, tv;
+    if ((st = encode_qkv_map(&tq, Q, BH, N, d)) != ATTN_OK || (st = encode_qkv_map(&tk, K, BH, N, d)) != ATTN_OK ||
+        (st = encode_qkv_map(&tv, V, BH, N, d)) != ATTN_OK)
+        return st;
+
+    FwdParams p;
+    p.O = static_cast<__nv_bfloat16*>(O);
+    p.LSE = LSE;
+    p.error_word = dev->error_word;
+    p.timeout_ns = kDefaultTimeoutNs;
+    p.N = N;
+    p.BH = BH;
+    p.num_q_tiles = (N + kBr - 1) / kBr;
+    p.num_kv_tiles = (N + kBc - 1) / kBc;
+    p.num_pairs = (p.num_q_tiles + 1) / 2;
+    p.num_units = plan.num_units;
+    p.heads_per_group = plan.heads_per_group;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    if (d == 64)
+        return causal ? launch<64, true>(*dev, plan, tq, tk, tv, p, stream)
+                      : launch<64, false>(*dev, plan, tq, tk, tv, p, stream);
+    return causal ? launch<128, true>(*dev, plan, tq, tk, tv, p, stream)
+                  : launch<128, false>(*dev, plan, tq, tk, tv, p, stream);
+}
+
+extern "C" size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+    const size_t elems = static_cast<size_t>(B) * H * N * d;
+    const size_t t = (elems * 2 + 255) & ~static_cast<size_t>(255);
+    return 4 * t + static_cast<size_t>(B) * H * N * 4;
+}
+
+extern "C" int attn_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh, int B, int H,
+                             int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+    int st = check_args(Qh, Kh, Vh, Oh, LSEh, B, H, N, d, scale);
+    if (st != ATTN_OK && st != ATTN_ERR_MISALIGNED) return st;
+    if (!workspace || !aligned16(workspace)) return workspace ? ATTN_ERR_MISALIGNED : ATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < attn_fwd_host_workspace_bytes(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+    const size_t bytes = static_cast<size_t>(B) * H * N * d * 2;
+    const size_t t = (bytes + 255) & ~static_cast<size_t>(255);
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    void *q = w, *k = w + t, *v = w + 2 * t, *o = w + 3 * t;
+    float* lse = reinterpret_cast<float*>(w + 4 * t);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(q, Qh, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(k, Kh, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(v, Vh, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((st = attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream)) != ATTN_OK) return st;
+    if ((e = cudaMemcpyAsync(Oh, o, bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(LSEh, lse, static_cast<size_t>(B) * H * N * 4, cudaMemcpyDeviceToHost, stream)) !=
+            cudaSuccess)
+        return cuda_fail(e);
+    return ATTN_OK;
+}
+
+extern "C" int attn_last_device_error(cudaStream_t stream) {
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t word = 0;
+    if ((e = cudaMemcpy(&word, dev->error_word, sizeof word, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e);
+    if (word != 0 && (e = cudaMemset(dev->error_word, 0, sizeof word)) != cudaSuccess) return cuda_fail(e);
+    return word == kDevTimeout ? ATTN_ERR_TIMEOUT : (word == 0 ? ATTN_OK : ATTN_ERR_CUDA);
+}
+
+extern "C" int attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" const char* attn_strerror(int status) {
+    switch (status) {
+        case ATTN_OK: return "success";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, size out of range, or scale not finite and > 0)";
+        case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim must be 64 or 128; device must be sm_103)";
+        case ATTN_ERR_MISALIGNED: return "misaligned pointer (tensors need 16-byte alignment, LSE 4-byte)";
+        case ATTN_ERR_CUDA: return "CUDA call failed (see attn_last_cuda_error)";
+        case ATTN_ERR_TIMEOUT: return "a kernel-side wait ran out of time";
+        case ATTN_ERR_NO_DEVICE: return "no CUDA device";
+        default: return "unknown status";
+    }
+}
+
+// ----------------------------------------------------------------- test hook
+namespace elsattn {
+__global__ void wait_timeout_kernel(uint32_t* error_word, uint64_t timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const WaitCtx ctx{&abort_flag, error_word, timeout_ns};
+        mbar_wait(smem_u32(&bar), 0, ctx);  // nobody arrives: gives up after timeout_ns
+    }
+    __syncthreads();
+}
+}  // namespace elsattn
+
+extern "C" int attn_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t stream) {
+    if (timeout_ns == 0 || timeout_ns > 10000000000ull) return ATTN_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    int st = device_state(&dev);
+    if (st != ATTN_OK) return st;
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(dev->error_word, timeout_ns);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}

@@ -1,0 +1,450 @@
+// Fused exact-attention forward for sm_103a: TMA K/V ring -> tcgen05 S = Q K^T
+// into TMEM -> online softmax (exp2) in the softmax warpgroups -> P (bf16)
+// back into TMEM -> tcgen05 O += P V -> O / l and LSE to global memory.
+//
+// The loop structure is the streaming schedule of "From Attention Graph to
+// FlashAttention - A Memory-Centric Compilation Approach in AICF", section 5
+// ("for q_tile: load Q_tile; for kv_tile: load K_tile, load V_tile, compute
+// score, update softmax, accumulate output"), mapped onto one GB300 SM:
+//
+//   warp 0 (one lane)   TMA producer: Q tiles once per unit, then K_j, V_j
+//                       into a ring of shared-memory stages.
+//   warp 1 (one lane)   tcgen05.mma issuer; warp 1 also owns the TMEM
+//                       allocation.
+//   warps 4-7, 8-11     softmax warpgroups, one per resident query tile; thread
+//                       r owns query row r (TMEM lane r) of its tile.
+//
+// Two query tiles (Q0, Q1) share every K/V tile.  The MMA warp interleaves
+// them so that the tensor core works on one tile while the softmax of the
+// other runs ("fine-grained communication-computation overlap" in the AttenIO
+// abstract, here between TMA, the tensor core and the softmax warps):
+//     S0_j = Q0 K_j^T ; O1 += P1_{j-1} V_{j-1} ; S1_j = Q1 K_j^T ; O0 += P0_j V_j
+//
+// TMEM columns: [0,128) S0 | [128,256) S1 | [256,256+d) O0 | [256+d,256+2d) O1.
+// P_t (bf16, two per column) is written over the first 64 columns of S_t once
+// the softmax has read S_t into registers.  The next S_t = Q_t K^T is issued
+// after O_t += P_t V has been issued; tcgen05.mma operations of one thread run
+// in issue order on the SM's tensor core.
+//
+// Online softmax (the "streaming reformulation" of the IO-Aware Algorithms
+// page): per row, a reference maximum m (log2 units, scale folded in) and a
+// running sum l.  A tile whose row maximum exceeds m by more than
+// kRescaleLog2 moves m up and rescales l and the O accumulator by
+// 2^(m_old - m_new); smaller increases keep the stale m (the terms stay below
+// 2^kRescaleLog2 and the final O / l and LSE are unchanged by the choice of
+// m), which makes the O rescale rare after the first tiles.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "plan.h"
+#include "sm103_ptx.cuh"
+
+namespace elsattn {
+
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.693147180559945309f;
+
+struct FwdParams {
+    __nv_bfloat16* O;      // [BH, N, d]
+    float* LSE;            // [BH, N]
+    uint32_t* error_word;  // device error word (first error wins)
+    uint64_t timeout_ns;   // limit for any single wait
+    int N;
+    int BH;
+    int num_q_tiles;       // ceil(N / kBr)
+    int num_kv_tiles;      // ceil(N / kBc)
+    int num_pairs;         // ceil(num_q_tiles / 2): units per (batch, head)
+    int num_units;         // BH * num_pairs
+    int heads_per_group;   // causal schedule only
+    float scale_log2;      // scale * log2(e)
+};
+
+struct UnitInfo {
+    int bh;
+    int q0;      // first query tile of the pair (second is q0 + 1)
+    int n[2];    // K/V tiles each query tile visits
+};
+
+// Unit order.  Non-causal: head-major, so the CTAs running at the same time
+// read the K/V of few heads and share them in L2.  Causal: heads are taken in
+// groups; inside a group the heaviest query tiles (most visible keys) go first
+// and the heads of the group interleave, which keeps the L2 working set to a
+// group's K/V while starting long units early.
+template <bool CAUSAL>
+__device__ __forceinline__ UnitInfo decode_unit(int u, const FwdParams& p) {
+    UnitInfo ui;
+    int pair;
+    if (!CAUSAL) {
+        ui.bh = u / p.num_pairs;
+        pair = u - ui.bh * p.num_pairs;
+    } else {
+        const int G = p.heads_per_group;
+        const int g = u / (G * p.num_pairs);
+        const int r = u - g * G * p.num_pairs;
+        const int heads_here = min(G, p.BH - g * G);
+        const int rank = r / heads_here;
+        pair = p.num_pairs - 1 - rank;
+        ui.bh = g * G + (r - rank * heads_here);
+    }
+    ui.q0 = 2 * pair;
+    for (int t = 0; t < 2; ++t) {
+        const int qt = ui.q0 + t;
+        ui.n[t] = CAUSAL ? min(qt + 1, p.num_kv_tiles) : p.num_kv_tiles;
+    }
+    return ui;
+}
+
+template <int D>
+struct SmemLayout {
+    static constexpr int kTile = tile_bytes(D);
+    static constexpr int kStages = kv_stages_for(D);
+    static constexpr int kQOff = 0;
+    static constexpr int kRingOff = kQTiles * kTile;
+    static constexpr int kBarOff = kRingOff + kStages * kTile;
+    // barrier indices
+    static constexpr int kKvFull = 0;
+    static constexpr int kKvEmpty = kKvFull + kStages;
+    static constexpr int kQFull = kKvEmpty + kStages;   // [2]
+    static constexpr int kQEmpty = kQFull + 2;          // [2]
+    static constexpr int kSFull = kQEmpty + 2;          // [2]
+    static constexpr int kPFull = kSFull + 2;           // [2]
+    static constexpr int kOFull = kPFull + 2;           // [2]
+    static constexpr int kOEmpty = kOFull + 2;          // [2]
+    static constexpr int kDrain = kOEmpty + 2;
+    static constexpr int kNumBars = kDrain + 1;
+    static constexpr int kFlagsOff = kBarOff + kNumBars * 8;  // tmem base slot, abort flag
+    static constexpr int kBytes = kFlagsOff + 16;
+    static_assert(kBytes + 1024 <= smem_bytes_for(D), "shared memory layout exceeds the plan");
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+    using L = SmemLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t bar0 = s_base + L::kBarOff;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kFlagsOff);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::kFlagsOff + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const WaitCtx ctx{abort_flag, p.error_word, p.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0u;
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(bar(L::kKvFull + s), 1);
+            mbar_init(bar(L::kKvEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(L::kQFull + t), 1);
+            mbar_init(bar(L::kQEmpty + t), 1);
+            mbar_init(bar(L::kSFull + t), 1);
+            mbar_init(bar(L::kPFull + t), 128);
+            mbar_init(bar(L::kOFull + t), 1);
+            mbar_init(bar(L::kOEmpty + t), 128);
+        }
+        mbar_init(bar(L::kDrain), 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------------------ TMA producer
+        uint32_t kv_idx = 0;
+        uint32_t ul = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
+            const UnitInfo ui = decode_unit<CAUSAL>(u, p);
+            for (int t = 0; t < 2 && ok; ++t) {
+                ok = mbar_wait(bar(L::kQEmpty + t), (ul & 1u) ^ 1u, ctx);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTile);
+                const uint32_t dst = s_base + L::kQOff + t * L::kTile;
+#pragma unroll
+                for (int b = 0; b < D / 64; ++b)
+                    tma_load_3d(dst + b * (kBr * 128), &tmap_q, bar(L::kQFull + t), b * 64, (ui.q0 + t) * kBr, ui.bh);
+            }
+            const int n1 = ui.n[1];
+            for (int j = 0; j < n1 && ok; ++j) {
+#pragma unroll
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint32_t s = kv_idx % L::kStages;
+                    ok = mbar_wait(bar(L::kKvEmpty + s), ((kv_idx / L::kStages) & 1u) ^ 1u, ctx);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(L::kKvFull + s), L::kTile);
+                    const uint32_t dst = s_base + L::kRingOff + s * L::kTile;
+                    const CUtensorMap* tm = kv == 0 ? &tmap_k : &tmap_v;
+#pragma unroll
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(dst + b * (kBc * 128), tm, bar(L::kKvFull + s), b * 64, j * kBc, ui.bh);
+                    ++kv_idx;
+                }
+            }
+        }
+        if (!ok) {
+            // Abort: wait (bounded) for the copies still in flight before the
+            // CTA's shared memory is released.
+            const uint32_t first = kv_idx > static_cast<uint32_t>(L::kStages) ? kv_idx - L::kStages : 0u;
+            for (uint32_t i = first; i < kv_idx; ++i)
+                mbar_wait_drain(bar(L::kKvFull + i % L::kStages), (i / L::kStages) & 1u, 50000000ull);
+            if (ul > 0 || kv_idx > 0)
+                for (int t = 0; t < 2; ++t) mbar_wait_drain(bar(L::kQFull + t), (ul & 1u), 1000000ull);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc_s = make_idesc_bf16_f32(kBr, kBc, false, false);
+        constexpr uint32_t idesc_o = make_idesc_bf16_f32(kBr, D, false, true);
+        uint32_t kv_idx = 0;
+        uint32_t ul = 0;
+        uint32_t p_cnt[2] = {0u, 0u};
+        bool ok = true;
+        // S_t = Q_t K^T from ring slot `slot`.
+        auto gemm_s = [&](int t, uint32_t slot) {
+            const uint32_t qa = s_base + L::kQOff + t * L::kTile;
+            const uint32_t kb = s_base + L::kRingOff + slot * L::kTile;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * (kBr * 128) + (kk & 3) * 32;
+                mma_ss(tmem + t * kBc, make_smem_desc_sw128(qa + off, 16, 1024),
+                       make_smem_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            }
+        };
+        // O_t (+)= P_t V from ring slot `slot`; P_t is read from TMEM.
+        auto gemm_o = [&](int t, uint32_t slot, bool accumulate) {
+            const uint32_t vb = s_base + L::kRingOff + slot * L::kTile;
+#pragma unroll
+            for (int kk = 0; kk < kBc / 16; ++kk) {
+                mma_ts(tmem + 2 * kBc + t * D, tmem + t * kBc + kk * 8,
+                       make_smem_desc_sw128(vb + kk * 16 * 128, kBc * 128, 1024), idesc_o,
+                       (accumulate || kk > 0) ? 1u : 0u);
+            }
+        };
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
+            const UnitInfo ui = decode_unit<CAUSAL>(u, p);
+            const int n0 = ui.n[0], n1 = ui.n[1];
+            const uint32_t base = kv_idx;
+            ok = mbar_wait(bar(L::kQFull + 0), ul & 1u, ctx) && mbar_wait(bar(L::kQFull + 1), ul & 1u, ctx);
+            tc_fence_after_sync();
+            // O_t += P_t V_j, with the waits it needs.
+            auto pv = [&](int t, int j) -> bool {
+                const uint32_t vidx = base + 2u * j + 1u;
+                const uint32_t vs = vidx % L::kStages;
+                if (t == 0 || j >= n0) {  // first use of V_j
+                    if (!mbar_wait(bar(L::kKvFull + vs), (vidx / L::kStages) & 1u, ctx)) return false;
+                }
+                if (!mbar_wait(bar(L::kPFull + t), p_cnt[t] & 1u, ctx)) return false;
+                ++p_cnt[t];
+                if (j == 0 && !mbar_wait(bar(L::kOEmpty + t), (ul & 1u) ^ 1u, ctx)) return false;
+                tc_fence_after_sync();
+                gemm_o(t, vs, j > 0);
+                if (t == 1) mma_commit(bar(L::kKvEmpty + vs));  // V_j's last reader
+                if (j == ui.n[t] - 1) mma_commit(bar(L::kOFull + t));
+                return true;
+            };
+            for (int j = 0; j < n1 && ok; ++j) {
+                const uint32_t kidx = base + 2u * j;
+                const uint32_t ks = kidx % L::kStages;
+                if (!(ok = mbar_wait(bar(L::kKvFull + ks), (kidx / L::kStages) & 1u, ctx))) break;
+                tc_fence_after_sync();
+                if (j < n0) {
+                    gemm_s(0, ks);
+                    mma_commit(bar(L::kSFull + 0));
+                    if (j == n0 - 1) mma_commit(bar(L::kQEmpty + 0));
+                }
+                if (j > 0 && !(ok = pv(1, j - 1))) break;
+                gemm_s(1, ks);
+                mma_commit(bar(L::kSFull + 1));
+                mma_commit(bar(L::kKvEmpty + ks));
+                if (j == n1 - 1) mma_commit(bar(L::kQEmpty + 1));
+                if (j < n0 && !(ok = pv(0, j))) break;
+            }
+            if (ok) ok = pv(1, n1 - 1);
+            kv_idx = base + 2u * n1;
+        }
+        // Make sure no MMA is still writing TMEM when it is released.
+        mma_commit(bar(L::kDrain));
+        mbar_wait_drain(bar(L::kDrain), 0, 1000000000ull);
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax warpgroups
+        const int t = (warp - 4) >> 2;          // query tile of this warpgroup
+        const int quad = warp & 3;              // TMEM lane quadrant this warp may access
+        const int rloc = quad * 32 + lane;      // row within the tile
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t t_s = tmem + lane_addr + t * kBc;
+        const uint32_t t_o = tmem + lane_addr + 2 * kBc + t * D;
+        const float sl2 = p.scale_log2;
+        uint32_t s_cnt = 0;
+        uint32_t ul = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
+            const UnitInfo ui = decode_unit<CAUSAL>(u, p);
+            const int qt = ui.q0 + t;
+            const int qrow = qt * kBr + rloc;
+            const int nt = ui.n[t];
+            float m_ref = -INFINITY;
+            float l = 0.f;
+            for (int j = 0; j < nt; ++j) {
+                ok = mbar_wait(bar(L::kSFull + t), s_cnt & 1u, ctx);
+                ++s_cnt;
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after_sync();
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tmem_ld32(t_s + 0, r0);
+                tmem_ld32(t_s + 32, r1);
+                tmem_ld32(t_s + 64, r2);
+                tmem_ld32(t_s + 96, r3);
+                tmem_wait_ld(r0);
+                tmem_wait_ld(r1);
+                tmem_wait_ld(r2);
+                tmem_wait_ld(r3);
+                float* s0 = reinterpret_cast<float*>(r0);
+                float* s1 = reinterpret_cast<float*>(r1);
+                float* s2 = reinterpret_cast<float*>(r2);
+                float* s3 = reinterpret_cast<float*>(r3);
+                const int key0 = j * kBc;
+                const bool need_mask = (key0 + kBc > p.N) || (CAUSAL && j >= qt);
+                if (need_mask) {
+                    const int lim = CAUSAL ? min(p.N - 1, qrow) : p.N - 1;  // last visible key
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        if (key0 + c > lim) s0[c] = -INFINITY;
+                        if (key0 + 32 + c > lim) s1[c] = -INFINITY;
+                        if (key0 + 64 + c > lim) s2[c] = -INFINITY;
+                        if (key0 + 96 + c > lim) s3[c] = -INFINITY;
+                    }
+                }
+                float mx0 = s0[0], mx1 = s1[0], mx2 = s2[0], mx3 = s3[0];
+#pragma unroll
+                for (int c = 1; c < 32; ++c) {
+                    mx0 = fmaxf(mx0, s0[c]);
+                    mx1 = fmaxf(mx1, s1[c]);
+                    mx2 = fmaxf(mx2, s2[c]);
+                    mx3 = fmaxf(mx3, s3[c]);
+                }
+                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const bool grow = m_tile > m_ref + kRescaleLog2;
+                float alpha = 1.f;
+                if (grow) {
+                    alpha = ex2_approx(m_ref - m_tile);  // 0 on the first tile
+                    m_ref = m_tile;
+                }
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                l *= alpha;
+                // P = 2^(s*scale*log2e - m), packed as bf16 pairs over the first
+                // 64 columns of S_t.
+                uint32_t pk[32];
+                float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float a = ex2_approx(fmaf(s0[2 * c], sl2, -m_use));
+                    const float b = ex2_approx(fmaf(s0[2 * c + 1], sl2, -m_use));
+                    acc0 += a;
+                    acc1 += b;
+                    pk[c] = pack_bf16x2(a, b);
+                }
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float a = ex2_approx(fmaf(s1[2 * c], sl2, -m_use));
+                    const float b = ex2_approx(fmaf(s1[2 * c + 1], sl2, -m_use));
+                    acc0 += a;
+                    acc1 += b;
+                    pk[16 + c] = pack_bf16x2(a, b);
+                }
+                tmem_st32(t_s + 0, pk);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float a = ex2_approx(fmaf(s2[2 * c], sl2, -m_use));
+                    const float b = ex2_approx(fmaf(s2[2 * c + 1], sl2, -m_use));
+                    acc0 += a;
+                    acc1 += b;
+                    pk[c] = pack_bf16x2(a, b);
+                }
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float a = ex2_approx(fmaf(s3[2 * c], sl2, -m_use));
+                    const float b = ex2_approx(fmaf(s3[2 * c + 1], sl2, -m_use));
+                    acc0 += a;
+                    acc1 += b;
+                    pk[16 + c] = pack_bf16x2(a, b);
+                }
+                tmem_st32(t_s + 32, pk);
+                l += acc0 + acc1;
+                // Rescale the O accumulator when this row's reference max moved.
+                // O_t's previous P V has completed: it was issued before this
+                // S_t, whose completion was just observed.
+                if (__any_sync(0xffffffffu, grow && j > 0)) {
+#pragma unroll 1
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(t_o + c, o);
+                        tmem_wait_ld(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(t_o + c, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::kPFull + t));
+            }
+            if (!ok) break;
+            // Epilogue: O = O_acc / l -> bf16, LSE = ln 2 * (m + log2 l).
+            ok = mbar_wait(bar(L::kOFull + t), ul & 1u, ctx);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after_sync();
+            const float inv_l = 1.f / l;
+            const bool row_ok = qrow < p.N;
+            const size_t grow_idx = static_cast<size_t>(ui.bh) * p.N + (row_ok ? qrow : 0);
+            uint4* orow = reinterpret_cast<uint4*>(p.O + grow_idx * D);
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(t_o + c, o);
+                tmem_wait_ld(o);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        orow[c / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (row_ok) {
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                p.LSE[grow_idx] = (m_use + lg2_approx(l)) * kLn2;
+            }
+            tc_fence_before_sync();
+            mbar_arrive(bar(L::kOEmpty + t));
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace elsattn

@@ -1,0 +1,119 @@
+// Tile planner: an I/O count of the two tall-and-skinny products of
+// attention against the on-chip capacity of one sm_103 SM.
+//
+// The AttenIO abstract ("I/O Analysis is All You Need: An I/O Analysis for
+// Long-Sequence Attention", ASPLOS 2026) derives its tiling from an I/O
+// analysis of tall-and-skinny matrix multiplication; the IO-Aware Algorithms
+// page gives the tiling rule behind it (staging a tile on chip and reusing it
+// S times divides the GEMM traffic 2MNK by S).  For one (batch, head), with
+// q query tiles of Br rows resident per CTA and K/V streamed in tiles of Bc
+// keys:
+//     Q is read once                     N d
+//     K and V are streamed once per CTA  2 N d * ceil(N / (q Br))
+//     O is written once                  N d
+// so the streamed K/V term shrinks with the resident query rows q Br, and the
+// best tiling is the largest q Br that fits:
+//     shared memory  q Br d 2B + stages Bc d 2B   <= 227 KB   (stages >= 3)
+//     tensor memory  q (Bc + d) fp32 columns       <= 512     (S and O per tile)
+// with Br = 128 (one TMEM lane per query row, tcgen05 M = 128).  The search
+// runs over every capacity-feasible (q, Bc); the plan reports the overall
+// I/O optimum and selects the least-traffic tiling among those the kernel
+// is compiled for (q = 2 query tiles in ping-pong, Bc = 128).  At d = 128 the
+// two coincide; at d = 64 the optimum is q = 4, Bc = 64, which the kernel
+// does not implement.
+#include <cmath>
+
+#include "../../include/exact_attn.h"
+#include "plan.h"
+
+namespace elsattn {
+
+struct Candidate {
+    int q, Bc, stages;
+    double l2_bytes;
+    bool fits;
+};
+
+// K/V bytes the CTAs stream from L2 for one (batch, head), plus Q read and O written.
+static double l2_traffic_per_head(int N, int d, int q, int causal) {
+    const double nd = static_cast<double>(N) * d;
+    const double units = std::ceil(static_cast<double>(N) / (q * kBr));
+    // causal: a unit streams only the keys up to its last query row; on average half.
+    const double kv_passes = causal ? 0.5 * (units + 1) : units;
+    return 2.0 * (nd + 2.0 * nd * kv_passes + nd);
+}
+
+static Candidate evaluate(int N, int d, int causal, int q, int Bc) {
+    Candidate c{q, Bc, 0, 0.0, false};
+    const int q_bytes = q * kBr * d * 2;
+    const int stage_bytes = Bc * d * 2;
+    const int tmem = q * (Bc + d);
+    c.stages = (kSmemLimit - kSmemReserve - q_bytes) / stage_bytes;
+    c.fits = tmem <= 512 && c.stages >= 3;
+    c.l2_bytes = l2_traffic_per_head(N, d, q, causal);
+    return c;
+}
+
+}  // namespace elsattn
+
+using namespace elsattn;
+
+extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out) {
+    if (!out || B < 1 || H < 1 || N < 1 || num_sms < 1) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * H * N >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+
+    // Search the tilings the capacity allows; keep the one with least traffic
+    // overall, and the one with least traffic among the compiled variants.
+    Candidate best{0, 0, 0, 0.0, false}, chosen{0, 0, 0, 0.0, false};
+    auto better = [](const Candidate& c, const Candidate& b) {
+        // less traffic first, then the larger K/V tile (fewer pipeline steps)
+        return !b.fits || c.l2_bytes < b.l2_bytes * (1 - 1e-12) ||
+               (std::fabs(c.l2_bytes - b.l2_bytes) <= b.l2_bytes * 1e-12 && c.Bc > b.Bc);
+    };
+    const int qs[] = {1, 2, 3, 4};
+    const int bcs[] = {64, 128, 256};
+    for (int q : qs)
+        for (int bc : bcs) {
+            const Candidate c = evaluate(N, d, causal, q, bc);
+            if (!c.fits) continue;
+            if (better(c, best)) best = c;
+            if (q == kQTiles && bc == kBc && better(c, chosen)) chosen = c;
+        }
+    if (!chosen.fits) return ATTN_ERR_UNSUPPORTED;
+    out->io_opt_q_tiles = best.q;
+    out->io_opt_Bc = best.Bc;
+    out->io_opt_l2_bytes = static_cast<double>(B) * H * best.l2_bytes + static_cast<double>(B) * H * 4.0 * N;
+
+    const long long BH = static_cast<long long>(B) * H;
+    const int q_tiles = (N + kBr - 1) / kBr;
+    const int pairs = (q_tiles + kQTiles - 1) / kQTiles;
+    const long long units = BH * pairs;
+
+    out->Br = kBr;
+    out->Bc = kBc;
+    out->q_tiles = kQTiles;
+    out->kv_stages = kv_stages_for(d);
+    out->tmem_cols = kTmemCols;
+    out->smem_bytes = smem_bytes_for(d);
+    out->threads = kThreads;
+    out->num_units = static_cast<int>(units);
+    out->grid = static_cast<int>(units < num_sms ? units : num_sms);
+
+    // Causal scheduling groups: as many heads as keep their K and V within
+    // about half of the 126 MB L2.
+    const double kv_head_bytes = 2.0 * N * d * 2.0;
+    long long g = static_cast<long long>(64.0 * 1024 * 1024 / kv_head_bytes);
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    out->heads_per_group = static_cast<int>(g);
+
+    const double nd = static_cast<double>(N) * d;
+    out->flops = 4.0 * BH * static_cast<double>(N) * N * d * (causal ? 0.5 : 1.0);
+    out->io_bytes = BH * (2.0 * 4.0 * nd + 4.0 * N);
+    out->l2_bytes = BH * l2_traffic_per_head(N, d, kQTiles, causal) + BH * 4.0 * N;
+    // HBM: each head's K/V comes from HBM once when the heads in flight fit in
+    // L2 (the schedule keeps them together), so the model is the I/O bound.
+    out->hbm_bytes = out->io_bytes;
+    return ATTN_OK;
+}

@@ -1,0 +1,138 @@
+/*
+ * exact_attn.h - C ABI of the GB300 (sm_103a) exact self-attention forward.
+ *
+ * The operation is the attention graph of "From Attention Graph to
+ * FlashAttention - A Memory-Centric Compilation Approach in AICF", section 1
+ * (Introduction):
+ *     Scores = Q x K^T ; Scores = Mask(Scores) ; Scores = Softmax(Scores) ;
+ *     Output = Scores x V
+ * with the scores multiplied by `scale`, plus the per-row log-sum-exp
+ *     LSE_i = ln sum_j exp(scale * q_i . k_j)   (over the keys the mask keeps).
+ * It is computed as the streaming pass of section 3 of that page ("load Q
+ * tile, stream K/V tiles, compute partial scores, online softmax update,
+ * accumulate output"): the N x N score and probability matrices never reach
+ * device memory.  The library is the `flash_attention(Q, K, V)` call of
+ * section 4 of the same page, with the optional mask of section 5 as a flag.
+ *
+ * Conventions for every entry point:
+ *   - Q, K, V, O are bf16 tensors laid out [B, H, N, d], contiguous, d fastest;
+ *     LSE is fp32 [B, H, N].  All five live in device memory, are owned by the
+ *     caller and must not overlap (not checked).
+ *   - causal != 0 keeps key j for query i iff j <= i; masked scores are
+ *     -infinity, i.e. they drop out of the softmax.
+ *   - Calls are asynchronous on `stream` and never synchronise it.
+ *   - Errors are returned as attn_status codes; nothing aborts or throws
+ *     across this boundary.
+ */
+#ifndef EXACT_ATTN_H
+#define EXACT_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, non-finite or non-positive scale */
+    ATTN_ERR_UNSUPPORTED = 2,  /* head dim other than 64/128, or a device other than sm_103 */
+    ATTN_ERR_MISALIGNED = 3,   /* a tensor base address is not 16-byte aligned */
+    ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed: see attn_last_cuda_error() */
+    ATTN_ERR_TIMEOUT = 5,      /* a kernel-side wait ran out of time (reported by attn_last_device_error) */
+    ATTN_ERR_NO_DEVICE = 6     /* no CUDA device is visible */
+} attn_status;
+
+/*
+ * Tile plan chosen by the I/O-count planner (see attn_plan).  Sizes are in
+ * elements unless named *_bytes.
+ */
+typedef struct {
+    int Br;               /* query rows per tile (the tcgen05 M dimension) */
+    int Bc;               /* keys per streamed K/V tile */
+    int q_tiles;          /* query tiles resident per CTA (they share every K/V tile) */
+    int kv_stages;        /* depth of the shared-memory K/V ring (one tile per stage) */
+    int tmem_cols;        /* tensor-memory columns allocated per CTA */
+    int smem_bytes;       /* dynamic shared memory per CTA */
+    int threads;          /* threads per CTA */
+    int num_units;        /* work units: (batch*head, group of q_tiles query tiles) */
+    int grid;             /* persistent CTAs launched (<= SM count) */
+    int heads_per_group;  /* causal schedule: heads interleaved per scheduling group */
+    double flops;         /* 4*B*H*N^2*d, halved when causal */
+    double io_bytes;      /* Theta(N*d) bound: bf16 Q,K,V read + bf16 O, fp32 LSE written once */
+    double l2_bytes;      /* modelled L2->SMEM traffic of the chosen tiling */
+    double hbm_bytes;     /* modelled HBM traffic of the chosen tiling and schedule */
+    int io_opt_q_tiles;   /* the capacity-feasible tiling with least L2->SMEM traffic ... */
+    int io_opt_Bc;        /* ... (may be one the kernel is not compiled for) */
+    double io_opt_l2_bytes; /* its modelled L2->SMEM traffic */
+} attn_plan_t;
+
+/*
+ * attn_fwd - O = softmax(scale * Q K^T + mask) V and LSE, for B*H independent
+ * (batch, head) problems.
+ *   Q, K, V : const bf16 [B,H,N,d] device pointers, 16-byte aligned
+ *   O       : bf16 [B,H,N,d] device pointer, 16-byte aligned (written)
+ *   LSE     : fp32 [B,H,N] device pointer, 4-byte aligned (written; natural log)
+ *   B, H, N : >= 1 with B*H*N < 2^31;  d : 64 or 128
+ *   causal  : 0 = no mask, nonzero = causal mask (key j visible to query i iff j <= i)
+ *   scale   : finite, > 0 (typically 1/sqrt(d))
+ *   stream  : CUDA stream on the current device (0 = legacy default stream)
+ * Returns ATTN_OK when the launch was queued.  Kernel-side timeouts are
+ * reported later by attn_last_device_error().
+ */
+int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+             int causal, float scale, cudaStream_t stream);
+
+/*
+ * attn_fwd_host - the same operation on HOST buffers: copies Q, K, V to the
+ * device, runs attn_fwd and copies O and LSE back, all queued on `stream`
+ * (pinned host memory makes the copies asynchronous).  The caller synchronises
+ * the stream before reading O / LSE.
+ *   Qh, Kh, Vh, Oh, LSEh : host pointers with the layouts of attn_fwd
+ *   workspace            : device buffer of at least attn_fwd_host_workspace_bytes()
+ *                          bytes, 16-byte aligned, owned by the caller
+ */
+int attn_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh, int B, int H, int N,
+                  int d, int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Device bytes attn_fwd_host needs for its staging copies of Q, K, V, O, LSE. */
+size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * attn_plan - host only, launches nothing.  Fills *out with the tiling the
+ * planner derives from an I/O count of the two tall-and-skinny products
+ * (S = Q K^T and O = P V) against the shared- and tensor-memory capacity of an
+ * sm_103 SM (the "I/O-optimal tiling" of the AttenIO abstract, "I/O Analysis
+ * is All You Need", ASPLOS 2026).  num_sms <= 0 queries the current device.
+ */
+int attn_plan(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out);
+
+/*
+ * attn_last_device_error - synchronises `stream`, then reads and clears the
+ * current device's kernel error word.  Returns ATTN_OK or ATTN_ERR_TIMEOUT.
+ */
+int attn_last_device_error(cudaStream_t stream);
+
+/* The cudaError_t of the most recent ATTN_ERR_CUDA on this thread (0 if none). */
+int attn_last_cuda_error(void);
+
+/* A static, human-readable description of a status code. */
+const char* attn_strerror(int status);
+
+/*
+ * attn_debug_wait_timeout - test hook for the bounded-wait machinery: launches
+ * one CTA that waits on an mbarrier nobody arrives on, with the given limit in
+ * nanoseconds (<= 10 s).  The kernel gives up, records ATTN_ERR_TIMEOUT in the
+ * device error word and exits normally, so the context stays usable; read the
+ * result with attn_last_device_error().
+ */
+int attn_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTN_H */
