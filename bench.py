@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Throughput of the exact-attention forward on GB300, as one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}] [--workload NAME]
+
+A step is one full forward pass (one kernel launch) over the workload's whole
+batch: by default B=1, H=16, N=16384, d=128, non-causal, bf16 inputs already
+resident in device memory. Each timed step is bracketed by CUDA events on the
+launching stream; L2 is flushed (a 256 MiB write) between timed steps, outside
+the events. `e2e` times the same pass through the host-buffer C-ABI entry
+(attn_fwd_host): pinned host Q, K, V in, O and LSE out, copies included.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of query rows of the same workload.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (the forward pass shards into independent (batch, head)
+problems, so there is no data-path collective); rank 0 reports the units of
+all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak at N=16K, d=128"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "sm103_ptx.cuh", "plan.h", "attn_api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=None, help="named workload (default: the long-sequence headline case)")
+    ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer end-to-end leg")
+    ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-baseline sample")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- distributed helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def whole_job(units_per_rank: float, rank_seconds: list[float]) -> tuple[float, float]:
+    """(total units / slowest rank's seconds, slowest seconds): the aggregate over ranks."""
+    slowest = max(rank_seconds)
+    return units_per_rank * len(rank_seconds) / slowest, slowest
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- measurement helpers
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0.0)) or None, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, None, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_long_sequence_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu capture, or None if the
+    kernel sources changed since it was taken (or there is none)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm = []
+        reasons = set()
+        smax = None
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                smax = float(r[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[3:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def cpu_oracle_sample(w, target_seconds: float, seed: int = 0):
+    """Time the fp64 oracle on a bounded sample of query rows of workload `w`.
+
+    Returns (TFLOP/s, seconds, rows, threads, description). FLOPs of a sampled
+    row are counted as the GPU's are: 4*N*d per row non-causal (2*N*d causal,
+    the same half count), so the rate is comparable with the GPU number.
+    """
+    import numpy as np
+    import torch
+
+    import oracle
+    from exact_long_sequence_gb300 import workloads
+
+    oracle.build()
+    threads = os.cpu_count() or 1
+    # one (b, h) of the workload, seeded like the workload itself
+    q, k, v = workloads.make_inputs(1, 1, w.N, w.d, w.seed, w.qk_dist, w.v_dist)
+    flops_per_row = (2.0 if w.causal else 4.0) * w.N * w.d
+
+    def timed(rows):
+        r = workloads.sample_rows(1, w.N, rows, seed + w.seed).numpy()
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.causal, w.scale, rows=r, nthreads=threads)
+        return time.perf_counter() - t0, r.shape[1]
+
+    probe_rows = max(threads, 32)
+    dt, n = timed(probe_rows)
+    rows = int(min(w.N, max(probe_rows, probe_rows * target_seconds / max(dt, 1e-6))))
+    dt, n = timed(rows)
+    desc = (f"{n} random query rows of one (batch, head) of {w.name} (N={w.N}, d={w.d}, causal={w.causal}), "
+            f"fp64, {threads} threads; rate = {flops_per_row:.3g} FLOP per row / wall time")
+    return flops_per_row * n / dt / 1e12, dt, n, threads, desc
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    per_step = max(1.0, min(args.cpu_seconds, 90.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, per_step / 4)
+    vals, secs = [], []
+    desc, threads, rows = "", 0, 0
+    for _ in range(args.steps):
+        v, dt, rows, threads, desc = cpu_oracle_sample(w, per_step)
+        vals.append(v)
+        secs.append(dt)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, "none (host CPU)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, l2_note):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "scale": w.scale, "inputs": f"seeded synthetic ({w.qk_dist} Q,K; {w.v_dist} V), bf16",
+            "l2": l2_note, "parallelism": "replicas"}
+
+
+def run_gb300(args, w):
+    import torch
+
+    import exact_long_sequence_gb300 as ela
+    from exact_long_sequence_gb300 import _build
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (sm_103a); no CPU fallback exists")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(ela.LIB_PATH):
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    ela.load_library()
+
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    # Device-resident synthetic inputs with the workload's distributions (drawn on the GPU for speed).
+    q = torch.randn(shape, device=dev, generator=g)
+    k = torch.randn(shape, device=dev, generator=g)
+    v = torch.randn(shape, device=dev, generator=g) if w.v_dist == "normal" else torch.rand(shape, device=dev, generator=g) * 2 - 1
+    if w.qk_dist == "normal_spiky":
+        q = torch.where(torch.rand(shape, device=dev, generator=g) < 0.01, q * 10, q)
+        k = torch.where(torch.rand(shape, device=dev, generator=g) < 0.01, k * 10, k)
+    q, k, v = (t.to(torch.bfloat16).contiguous() for t in (q, k, v))
+    o = torch.empty_like(q)
+    lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    for _ in range(max(3, args.warmup)):
+        ela.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
+    torch.cuda.synchronize(dev)
+    if ela.last_device_error(stream) != ela.ATTN_OK:
+        raise SystemExit("kernel reported a device error during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            ela.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    if ela.last_device_error(stream) != ela.ATTN_OK:
+        raise SystemExit("kernel reported a device error during the timed steps")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    my_seconds = sum(step_ms) / 1e3
+    slowest = max_over_ranks(my_seconds, world, dev)
+    value = w.flops * args.steps * world / slowest / 1e12
+    ms_per_step = slowest * 1e3 / args.steps
+    kernel_ms = statistics.mean(step_ms)
+
+    # ------------------------------------------------------------- end to end through the host-buffer entry
+    e2e = None
+    if not args.skip_e2e:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty_like(qh).pin_memory()
+        lh = torch.empty(shape[:3], dtype=torch.float32).pin_memory()
+        ws = torch.empty(ela.host_workspace_bytes(*shape), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            ela.attn_fwd_host(qh, kh, vh, causal=w.causal, scale=w.scale, out_h=oh, lse_h=lh, workspace=ws,
+                              stream=stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e_ms = []
+        for _ in range(max(3, args.steps // 2)):
+            flush.zero_()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            ela.attn_fwd_host(qh, kh, vh, causal=w.causal, scale=w.scale, out_h=oh, lse_h=lh, workspace=ws,
+                              stream=stream)
+            stream.synchronize()
+            e_ms.append((time.perf_counter() - t0) * 1e3)
+        e_slow = max_over_ranks(sum(e_ms) / 1e3, world, dev)
+        nbytes = q.numel() * 2
+        e2e = {"value": w.flops * len(e_ms) * world / e_slow / 1e12, "unit": UNIT,
+               "ms_per_step": e_slow * 1e3 / len(e_ms),
+               "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes + lse.numel() * 4,
+               "api": "attn_fwd_host (pinned host buffers, copies + kernel on one stream, wall clock)"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_sustained, peak_kind = read_peaks()
+    achieved = w.flops / (kernel_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                "peak_kind": f"{peak_kind} dense bf16 burst (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                else "fallback dense bf16 burst",
+                "traffic": recorded_traffic(w.name),
+                "algorithmic_flops_per_launch": w.flops, "kernel_ms": kernel_ms,
+                "io_bound_bytes": w.io_bytes}
+    if peak_sustained:
+        roofline["frac_of_sustained"] = achieved / peak_sustained
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"),
+        "roofline": roofline,
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.skip_cpu and world == 1:
+        v_cpu, dt, rows, threads, desc = cpu_oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+                                "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from exact_long_sequence_gb300 import workloads
+
+    name = args.workload or workloads.HEADLINE
+    if name not in workloads.WORKLOADS:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(workloads.WORKLOADS)}")
+    w = workloads.WORKLOADS[name]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gb300(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

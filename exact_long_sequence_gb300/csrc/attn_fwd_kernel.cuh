@@ -96,6 +96,16 @@ __device__ __forceinline__ UnitInfo decode_unit(int u, const FwdParams& p) {
     return ui;
 }
 
+// Position in the shared-memory K/V ring: stage index and the parity of the
+// stage's current fill.
+struct RingPos {
+    uint32_t stage;
+    uint32_t phase;
+    __device__ __forceinline__ RingPos next(uint32_t stages) const {
+        return stage + 1 == stages ? RingPos{0u, phase ^ 1u} : RingPos{stage + 1, phase};
+    }
+};
+
 template <int D>
 struct SmemLayout {
     static constexpr int kTile = tile_bytes(D);
@@ -167,11 +177,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer
-        uint32_t kv_idx = 0;
+        RingPos pos{0u, 0u};      // next ring position to fill
+        uint32_t issued = 0;      // ring fills issued so far
         uint32_t ul = 0;
+        uint32_t q_issued = 0;    // bit t: a Q_t load of local unit (ul) is in flight
         bool ok = true;
         for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
             const UnitInfo ui = decode_unit<CAUSAL>(u, p);
+            q_issued = 0;
             for (int t = 0; t < 2 && ok; ++t) {
                 ok = mbar_wait(bar(L::kQEmpty + t), (ul & 1u) ^ 1u, ctx);
                 if (!ok) break;
@@ -180,106 +193,127 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
                 for (int b = 0; b < D / 64; ++b)
                     tma_load_3d(dst + b * (kBr * 128), &tmap_q, bar(L::kQFull + t), b * 64, (ui.q0 + t) * kBr, ui.bh);
+                q_issued |= 1u << t;
             }
             const int n1 = ui.n[1];
             for (int j = 0; j < n1 && ok; ++j) {
 #pragma unroll
                 for (int kv = 0; kv < 2; ++kv) {
-                    const uint32_t s = kv_idx % L::kStages;
-                    ok = mbar_wait(bar(L::kKvEmpty + s), ((kv_idx / L::kStages) & 1u) ^ 1u, ctx);
+                    ok = mbar_wait(bar(L::kKvEmpty + pos.stage), pos.phase ^ 1u, ctx);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar(L::kKvFull + s), L::kTile);
-                    const uint32_t dst = s_base + L::kRingOff + s * L::kTile;
+                    mbar_arrive_expect_tx(bar(L::kKvFull + pos.stage), L::kTile);
+                    const uint32_t dst = s_base + L::kRingOff + pos.stage * L::kTile;
                     const CUtensorMap* tm = kv == 0 ? &tmap_k : &tmap_v;
 #pragma unroll
                     for (int b = 0; b < D / 64; ++b)
-                        tma_load_3d(dst + b * (kBc * 128), tm, bar(L::kKvFull + s), b * 64, j * kBc, ui.bh);
-                    ++kv_idx;
+                        tma_load_3d(dst + b * (kBc * 128), tm, bar(L::kKvFull + pos.stage), b * 64, j * kBc, ui.bh);
+                    pos = pos.next(L::kStages);
+                    ++issued;
                 }
             }
+            if (!ok) break;
         }
         if (!ok) {
             // Abort: wait (bounded) for the copies still in flight before the
-            // CTA's shared memory is released.
-            const uint32_t first = kv_idx > static_cast<uint32_t>(L::kStages) ? kv_idx - L::kStages : 0u;
-            for (uint32_t i = first; i < kv_idx; ++i)
-                mbar_wait_drain(bar(L::kKvFull + i % L::kStages), (i / L::kStages) & 1u, 50000000ull);
-            if (ul > 0 || kv_idx > 0)
-                for (int t = 0; t < 2; ++t) mbar_wait_drain(bar(L::kQFull + t), (ul & 1u), 1000000ull);
+            // CTA's shared memory is released.  The last min(issued, stages)
+            // fills are the only ones that can still be pending.
+            const uint32_t pending = issued < static_cast<uint32_t>(L::kStages) ? issued : L::kStages;
+            RingPos back = pos;
+            for (uint32_t i = 0; i < pending; ++i) {
+                back = back.stage == 0 ? RingPos{L::kStages - 1u, back.phase ^ 1u} : RingPos{back.stage - 1, back.phase};
+                mbar_wait_drain(bar(L::kKvFull + back.stage), back.phase, 50000000ull);
+            }
+            for (int t = 0; t < 2; ++t)
+                if (q_issued & (1u << t)) mbar_wait_drain(bar(L::kQFull + t), ul & 1u, 50000000ull);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        // The whole warp runs the loop and waits; one elected lane issues the
+        // MMAs and commits (a converged warp issues tcgen05.mma faster than a
+        // lone divergent lane).
         constexpr uint32_t idesc_s = make_idesc_bf16_f32(kBr, kBc, false, false);
         constexpr uint32_t idesc_o = make_idesc_bf16_f32(kBr, D, false, true);
-        uint32_t kv_idx = 0;
+        // The descriptor's start-address field holds (address >> 4), so a move
+        // inside shared memory is an add on the descriptor.
+        const uint64_t dq0 = make_smem_desc_sw128(s_base + L::kQOff, 16, 1024);
+        const uint64_t dk0 = make_smem_desc_sw128(s_base + L::kRingOff, 16, 1024);
+        const uint64_t dv0 = make_smem_desc_sw128(s_base + L::kRingOff, kBc * 128, 1024);
+        RingPos kpos{0u, 0u};  // ring position of the next unit's K_0
         uint32_t ul = 0;
-        uint32_t p_cnt[2] = {0u, 0u};
+        uint32_t p_phase[2] = {0u, 0u};
         bool ok = true;
-        // S_t = Q_t K^T from ring slot `slot`.
+        // S_t = Q_t K^T with K in ring stage `slot`.
         auto gemm_s = [&](int t, uint32_t slot) {
-            const uint32_t qa = s_base + L::kQOff + t * L::kTile;
-            const uint32_t kb = s_base + L::kRingOff + slot * L::kTile;
+            const uint64_t a = dq0 + static_cast<uint64_t>((t * L::kTile) >> 4);
+            const uint64_t b = dk0 + static_cast<uint64_t>((slot * L::kTile) >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * (kBr * 128) + (kk & 3) * 32;
-                mma_ss(tmem + t * kBc, make_smem_desc_sw128(qa + off, 16, 1024),
-                       make_smem_desc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBr * 128) + (kk & 3) * 32) >> 4);
+                mma_ss(tmem + t * kBc, a + off, b + off, idesc_s, kk > 0 ? 1u : 0u);
             }
         };
-        // O_t (+)= P_t V from ring slot `slot`; P_t is read from TMEM.
+        // O_t (+)= P_t V with V in ring stage `slot`; P_t is read from TMEM.
         auto gemm_o = [&](int t, uint32_t slot, bool accumulate) {
-            const uint32_t vb = s_base + L::kRingOff + slot * L::kTile;
+            const uint64_t b = dv0 + static_cast<uint64_t>((slot * L::kTile) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kBc / 16; ++kk) {
+            for (int kk = 0; kk < kBc / 16; ++kk)
                 mma_ts(tmem + 2 * kBc + t * D, tmem + t * kBc + kk * 8,
-                       make_smem_desc_sw128(vb + kk * 16 * 128, kBc * 128, 1024), idesc_o,
-                       (accumulate || kk > 0) ? 1u : 0u);
-            }
+                       b + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_o, (accumulate || kk > 0) ? 1u : 0u);
         };
         for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
             const UnitInfo ui = decode_unit<CAUSAL>(u, p);
             const int n0 = ui.n[0], n1 = ui.n[1];
-            const uint32_t base = kv_idx;
             ok = mbar_wait(bar(L::kQFull + 0), ul & 1u, ctx) && mbar_wait(bar(L::kQFull + 1), ul & 1u, ctx);
-            tc_fence_after_sync();
-            // O_t += P_t V_j, with the waits it needs.
-            auto pv = [&](int t, int j) -> bool {
-                const uint32_t vidx = base + 2u * j + 1u;
-                const uint32_t vs = vidx % L::kStages;
-                if (t == 0 || j >= n0) {  // first use of V_j
-                    if (!mbar_wait(bar(L::kKvFull + vs), (vidx / L::kStages) & 1u, ctx)) return false;
+            ok = __all_sync(0xffffffffu, ok);
+            // O_t += P_t V_j with V_j at ring position `vp`, with the waits it needs.
+            auto pv = [&](int t, int j, RingPos vp) -> bool {
+                bool w = true;
+                if (t == 0 || j >= n0)  // first use of V_j
+                    w = mbar_wait(bar(L::kKvFull + vp.stage), vp.phase, ctx);
+                w = w && mbar_wait(bar(L::kPFull + t), p_phase[t], ctx);
+                p_phase[t] ^= 1u;
+                if (j == 0) w = w && mbar_wait(bar(L::kOEmpty + t), (ul & 1u) ^ 1u, ctx);
+                if (!__all_sync(0xffffffffu, w)) return false;
+                tc_fence_after_sync();  // P_t and the O_t rescale came from other threads' tcgen05.st
+                if (elect_one()) {
+                    gemm_o(t, vp.stage, j > 0);
+                    if (t == 1) mma_commit(bar(L::kKvEmpty + vp.stage));  // V_j's last reader
+                    if (j == ui.n[t] - 1) mma_commit(bar(L::kOFull + t));
                 }
-                if (!mbar_wait(bar(L::kPFull + t), p_cnt[t] & 1u, ctx)) return false;
-                ++p_cnt[t];
-                if (j == 0 && !mbar_wait(bar(L::kOEmpty + t), (ul & 1u) ^ 1u, ctx)) return false;
-                tc_fence_after_sync();
-                gemm_o(t, vs, j > 0);
-                if (t == 1) mma_commit(bar(L::kKvEmpty + vs));  // V_j's last reader
-                if (j == ui.n[t] - 1) mma_commit(bar(L::kOFull + t));
+                __syncwarp();
                 return true;
             };
+            RingPos vpos = kpos.next(L::kStages);  // V_j
+            RingPos vprev = vpos;                  // V_{j-1}
             for (int j = 0; j < n1 && ok; ++j) {
-                const uint32_t kidx = base + 2u * j;
-                const uint32_t ks = kidx % L::kStages;
-                if (!(ok = mbar_wait(bar(L::kKvFull + ks), (kidx / L::kStages) & 1u, ctx))) break;
-                tc_fence_after_sync();
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kKvFull + kpos.stage), kpos.phase, ctx));
+                if (!ok) break;
                 if (j < n0) {
-                    gemm_s(0, ks);
-                    mma_commit(bar(L::kSFull + 0));
-                    if (j == n0 - 1) mma_commit(bar(L::kQEmpty + 0));
+                    if (elect_one()) {
+                        gemm_s(0, kpos.stage);
+                        mma_commit(bar(L::kSFull + 0));
+                        if (j == n0 - 1) mma_commit(bar(L::kQEmpty + 0));
+                    }
+                    __syncwarp();
                 }
-                if (j > 0 && !(ok = pv(1, j - 1))) break;
-                gemm_s(1, ks);
-                mma_commit(bar(L::kSFull + 1));
-                mma_commit(bar(L::kKvEmpty + ks));
-                if (j == n1 - 1) mma_commit(bar(L::kQEmpty + 1));
-                if (j < n0 && !(ok = pv(0, j))) break;
+                if (j > 0 && !(ok = pv(1, j - 1, vprev))) break;
+                if (elect_one()) {
+                    gemm_s(1, kpos.stage);
+                    mma_commit(bar(L::kSFull + 1));
+                    mma_commit(bar(L::kKvEmpty + kpos.stage));  // K_j's last reader
+                    if (j == n1 - 1) mma_commit(bar(L::kQEmpty + 1));
+                }
+                __syncwarp();
+                if (j < n0 && !(ok = pv(0, j, vpos))) break;
+                vprev = vpos;
+                kpos = kpos.next(L::kStages).next(L::kStages);
+                vpos = vpos.next(L::kStages).next(L::kStages);
             }
-            if (ok) ok = pv(1, n1 - 1);
-            kv_idx = base + 2u * n1;
+            if (ok) ok = pv(1, n1 - 1, vprev);
         }
         // Make sure no MMA is still writing TMEM when it is released.
-        mma_commit(bar(L::kDrain));
+        if (elect_one()) mma_commit(bar(L::kDrain));
+        __syncwarp();
         mbar_wait_drain(bar(L::kDrain), 0, 1000000000ull);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax warpgroups
@@ -331,15 +365,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         if (key0 + 96 + c > lim) s3[c] = -INFINITY;
                     }
                 }
-                float mx0 = s0[0], mx1 = s1[0], mx2 = s2[0], mx3 = s3[0];
+                // row max: 3-input max over the 128 scores, four independent chains
+                float mx0 = fmax3(s0[0], s0[1], s0[2]), mx1 = fmax3(s1[0], s1[1], s1[2]);
+                float mx2 = fmax3(s2[0], s2[1], s2[2]), mx3 = fmax3(s3[0], s3[1], s3[2]);
 #pragma unroll
-                for (int c = 1; c < 32; ++c) {
-                    mx0 = fmaxf(mx0, s0[c]);
-                    mx1 = fmaxf(mx1, s1[c]);
-                    mx2 = fmaxf(mx2, s2[c]);
-                    mx3 = fmaxf(mx3, s3[c]);
+                for (int c = 3; c < 31; c += 2) {
+                    mx0 = fmax3(mx0, s0[c], s0[c + 1]);
+                    mx1 = fmax3(mx1, s1[c], s1[c + 1]);
+                    mx2 = fmax3(mx2, s2[c], s2[c + 1]);
+                    mx3 = fmax3(mx3, s3[c], s3[c + 1]);
                 }
-                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                mx0 = fmax3(mx0, s0[31], mx1);
+                mx2 = fmax3(mx2, s2[31], mx3);
+                mx0 = fmax3(mx0, s1[31], fmaxf(mx2, s3[31]));
+                const float m_tile = mx0 * sl2;
                 const bool grow = m_tile > m_ref + kRescaleLog2;
                 float alpha = 1.f;
                 if (grow) {
@@ -349,44 +388,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
                 l *= alpha;
                 // P = 2^(s*scale*log2e - m), packed as bf16 pairs over the first
-                // 64 columns of S_t.
-                uint32_t pk[32];
-                float acc0 = 0.f, acc1 = 0.f;
+                // 64 columns of S_t, stored 16 columns (32 scores) at a time.
+                float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+                auto exp_chunk = [&](const float* sc, uint32_t col) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float a = ex2_approx(fmaf(s0[2 * c], sl2, -m_use));
-                    const float b = ex2_approx(fmaf(s0[2 * c + 1], sl2, -m_use));
-                    acc0 += a;
-                    acc1 += b;
-                    pk[c] = pack_bf16x2(a, b);
-                }
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float a = ex2_approx(fmaf(s1[2 * c], sl2, -m_use));
-                    const float b = ex2_approx(fmaf(s1[2 * c + 1], sl2, -m_use));
-                    acc0 += a;
-                    acc1 += b;
-                    pk[16 + c] = pack_bf16x2(a, b);
-                }
-                tmem_st32(t_s + 0, pk);
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float a = ex2_approx(fmaf(s2[2 * c], sl2, -m_use));
-                    const float b = ex2_approx(fmaf(s2[2 * c + 1], sl2, -m_use));
-                    acc0 += a;
-                    acc1 += b;
-                    pk[c] = pack_bf16x2(a, b);
-                }
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float a = ex2_approx(fmaf(s3[2 * c], sl2, -m_use));
-                    const float b = ex2_approx(fmaf(s3[2 * c + 1], sl2, -m_use));
-                    acc0 += a;
-                    acc1 += b;
-                    pk[16 + c] = pack_bf16x2(a, b);
-                }
-                tmem_st32(t_s + 32, pk);
-                l += acc0 + acc1;
+                    for (int c = 0; c < 16; c += 2) {
+                        const float a0 = ex2_approx(fmaf(sc[2 * c], sl2, -m_use));
+                        const float b0 = ex2_approx(fmaf(sc[2 * c + 1], sl2, -m_use));
+                        const float a1 = ex2_approx(fmaf(sc[2 * c + 2], sl2, -m_use));
+                        const float b1 = ex2_approx(fmaf(sc[2 * c + 3], sl2, -m_use));
+                        acc0 += a0;
+                        acc1 += b0;
+                        acc2 += a1;
+                        acc3 += b1;
+                        pk[c] = pack_bf16x2(a0, b0);
+                        pk[c + 1] = pack_bf16x2(a1, b1);
+                    }
+                    tmem_st16(t_s + col, pk);
+                };
+                exp_chunk(s0, 0);
+                exp_chunk(s1, 16);
+                exp_chunk(s2, 32);
+                exp_chunk(s3, 48);
+                l += (acc0 + acc1) + (acc2 + acc3);
                 // Rescale the O accumulator when this row's reference max moved.
                 // O_t's previous P V has completed: it was issued before this
                 // S_t, whose completion was just observed.
