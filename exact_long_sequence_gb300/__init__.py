@@ -41,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "attn_last_cuda_error",
     "attn_strerror",
     "attn_debug_wait_timeout",
+    "attn_fwd_noalloc",
 )
 
 
@@ -98,6 +99,8 @@ def load_library(path: str | None = None):
     lib.attn_strerror.restype = ctypes.c_char_p
     lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.attn_debug_wait_timeout.restype = i
+    lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    lib.attn_fwd_noalloc.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -152,6 +155,31 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
         st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                           B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
     _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_noalloc(q, k, v, out, lse, causal: bool = False, scale: float | None = None, stream=None):
+    """attn_fwd through the entry point that never allocates device memory.
+
+    For callers that cannot let the library cudaMalloc (their own pool owns all
+    of device memory, or their path cannot take cudaMalloc's implicit device
+    synchronisation): the kernel's error word lives in a fixed array compiled
+    into the library instead. The caller passes the outputs `out` (bf16, shaped
+    like q) and `lse` (fp32 [B, H, N]); calls that overlap on the GPU race on
+    the shared word, so serialise them.
+    """
+    lib = load_library()
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = default_scale(d)
+    for t in (q, k, v, out):
+        if t.shape != q.shape or not t.is_contiguous():
+            raise ValueError("q, k, v, out must be contiguous tensors of one [B, H, N, d] shape")
+    if lse.shape != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [B, H, N] tensor")
+    st = lib.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                              B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    _check(st, "attn_fwd_noalloc")
     return out, lse
 
 

@@ -261,3 +261,129 @@ extern "C" int attn_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t stream)
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
+
+// ----------------------------------------------------- allocation-free entry point
+// attn_fwd_noalloc runs the same kernel as attn_fwd for callers that must not
+// let the library allocate device memory: an application that reserves all of
+// device memory for its own pool up front (a server that hands the rest of HBM
+// to its cache), or one on a latency-critical path that cannot afford
+// cudaMalloc's implicit device synchronisation.  attn_fwd allocates one small
+// block per device on first use for the kernel's error word; here that word
+// lives in the fixed array below, compiled into the library, so the call never
+// allocates.  Every device that loads the library holds the array until exit.
+namespace elsattn {
+namespace {
+constexpr size_t kNoAllocScratchBytes = 256;           // the array's size: the most any call may use
+constexpr size_t kFwdScratchBytes = sizeof(uint32_t);  // what one forward launch uses: its error word
+}  // namespace
+}  // namespace elsattn
+
+static __device__ __align__(256) uint32_t els_noalloc_scratch[elsattn::kNoAllocScratchBytes / sizeof(uint32_t)];
+
+namespace elsattn {
+namespace {
+
+struct NoAllocDevice {
+    bool ready = false;
+    int num_sms = 0;
+    uint32_t* scratch = nullptr;  // device address of els_noalloc_scratch on this device
+};
+
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+
+// Once per device, with that device current: look up the device address of the
+// static array (its name in host code is only a stand-in, not an address the
+// kernel may use), and set the kernels' shared-memory limit.
+int noalloc_device(NoAllocDevice** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver) return ATTN_ERR_NO_DEVICE;
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    NoAllocDevice& s = g_noalloc_dev[dev];
+    if (!s.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return cuda_fail(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        void* ptr = nullptr;
+        if ((e = cudaGetSymbolAddress(&ptr, els_noalloc_scratch)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaFuncSetAttribute(attn_fwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      smem_bytes_for(64))) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      smem_bytes_for(64))) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn_fwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      smem_bytes_for(128))) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(attn_fwd_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      smem_bytes_for(128))) != cudaSuccess)
+            return cuda_fail(e);
+        s.scratch = static_cast<uint32_t*>(ptr);
+        s.ready = true;
+    }
+    *out = &s;
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace elsattn
+
+extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                                int N, int d, int causal, float scale, cudaStream_t stream) {
+    int st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
+    if (st != ATTN_OK) return st;
+    // The scratch a launch needs does not grow with B, H, N or d; it must fit the array.
+    if (kFwdScratchBytes > kNoAllocScratchBytes) return ATTN_ERR_INVALID_ARG;
+    NoAllocDevice* dev = nullptr;
+    if ((st = noalloc_device(&dev)) != ATTN_OK) return st;
+    attn_plan_t plan;
+    if ((st = attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan)) != ATTN_OK) return st;
+
+    const int BH = B * H;
+    CUtensorMap tq, tk, tv;
+    if ((st = encode_qkv_map(&tq, Q, BH, N, d)) != ATTN_OK || (st = encode_qkv_map(&tk, K, BH, N, d)) != ATTN_OK ||
+        (st = encode_qkv_map(&tv, V, BH, N, d)) != ATTN_OK)
+        return st;
+
+    // The array keeps the previous call's contents: the error word must start at zero.
+    cudaError_t e = cudaMemsetAsync(dev->scratch, 0, kFwdScratchBytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    FwdParams p;
+    p.O = static_cast<__nv_bfloat16*>(O);
+    p.LSE = LSE;
+    p.error_word = dev->scratch;
+    p.timeout_ns = kDefaultTimeoutNs;
+    p.N = N;
+    p.BH = BH;
+    p.num_q_tiles = (N + kBr - 1) / kBr;
+    p.num_kv_tiles = (N + kBc - 1) / kBc;
+    p.num_pairs = (p.num_q_tiles + 1) / 2;
+    p.num_units = plan.num_units;
+    p.heads_per_group = plan.heads_per_group;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    if (d == 64) {
+        if (causal)
+            attn_fwd_kernel<64, true><<<plan.grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
+        else
+            attn_fwd_kernel<64, false><<<plan.grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
+    } else {
+        if (causal)
+            attn_fwd_kernel<128, true><<<plan.grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
+        else
+            attn_fwd_kernel<128, false><<<plan.grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
+    }
+    e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}

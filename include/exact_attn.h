@@ -131,6 +131,34 @@ const char* attn_strerror(int status);
  */
 int attn_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 
+/*
+ * attn_fwd_noalloc - attn_fwd for callers that must not let the library
+ * allocate device memory: applications that reserve all of device memory for
+ * their own pool up front (such as a server handing the rest of HBM to its
+ * cache), or that cannot afford the implicit device synchronisation of
+ * cudaMalloc on their path.  The paper has no counterpart; it is an interface
+ * variant of attn_fwd with the same arguments, layouts and results.
+ *
+ * The kernel's only scratch memory is its 4-byte error word.  attn_fwd keeps
+ * it in a block the library allocates on first use; this entry point keeps it
+ * instead in a fixed 256-byte array compiled into the library (a static
+ * __device__ array), which every device that loads the library holds until
+ * exit.  The scratch a call needs does not grow with B, H, N or d; a
+ * requirement above 256 bytes would be rejected with ATTN_ERR_INVALID_ARG.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on a device also does that device's one-time set-up
+ *     (it looks up the array's device address and sets the kernel's
+ *     shared-memory limit); make that first call before any stream capture.
+ *   - Every call shares the one array and clears its error word before the
+ *     launch.  Calls that overlap on the GPU (other streams, other threads)
+ *     race on that word; serialise them.
+ *   - A kernel-side timeout is recorded in the array, not in the word that
+ *     attn_last_device_error reads.
+ * Returns the same status codes as attn_fwd.
+ */
+int attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                     int causal, float scale, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
