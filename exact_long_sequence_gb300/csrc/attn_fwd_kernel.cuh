@@ -119,14 +119,16 @@ struct SmemLayout {
     static constexpr int kQFull = kKvEmpty + kStages;   // [2]
     static constexpr int kQEmpty = kQFull + 2;          // [2]
     static constexpr int kSFull = kQEmpty + 2;          // [2]
-    static constexpr int kPFull = kSFull + 2;           // [2]
+    static constexpr int kPHalf = kSFull + 2;           // [2] first half of P_t (keys 0-63) stored, O_t rescaled
+    static constexpr int kPFull = kPHalf + 2;           // [2] second half of P_t stored
     static constexpr int kOFull = kPFull + 2;           // [2]
     static constexpr int kOEmpty = kOFull + 2;          // [2]
     static constexpr int kDrain = kOEmpty + 2;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr int kFlagsOff = kBarOff + kNumBars * 8;  // tmem base slot, abort flag
     static constexpr int kBytes = kFlagsOff + 16;
-    static_assert(kBytes + 1024 <= smem_bytes_for(D), "shared memory layout exceeds the plan");
+    static_assert(kNumBars == 2 * kStages + kFixedBarriers, "barrier count differs from the plan");
+    static_assert(kBytes + kSmemAlign <= smem_bytes_for(D), "shared memory layout exceeds the plan");
 };
 
 template <int D, bool CAUSAL>
@@ -156,6 +158,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             mbar_init(bar(L::kQFull + t), 1);
             mbar_init(bar(L::kQEmpty + t), 1);
             mbar_init(bar(L::kSFull + t), 1);
+            mbar_init(bar(L::kPHalf + t), 128);
             mbar_init(bar(L::kPFull + t), 128);
             mbar_init(bar(L::kOFull + t), 1);
             mbar_init(bar(L::kOEmpty + t), 128);
@@ -252,11 +255,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 mma_ss(tmem + t * kBc, a + off, b + off, idesc_s, kk > 0 ? 1u : 0u);
             }
         };
-        // O_t (+)= P_t V with V in ring stage `slot`; P_t is read from TMEM.
-        auto gemm_o = [&](int t, uint32_t slot, bool accumulate) {
+        // O_t (+)= P_t V over keys [64 half, 64 half + 64) with V in ring stage
+        // `slot`; P_t is read from TMEM.
+        auto gemm_o = [&](int t, uint32_t slot, int half, bool accumulate) {
             const uint64_t b = dv0 + static_cast<uint64_t>((slot * L::kTile) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kBc / 16; ++kk)
+            for (int kk = half * 4; kk < half * 4 + 4; ++kk)
                 mma_ts(tmem + 2 * kBc + t * D, tmem + t * kBc + kk * 8,
                        b + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_o, (accumulate || kk > 0) ? 1u : 0u);
         };
@@ -270,13 +274,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 bool w = true;
                 if (t == 0 || j >= n0)  // first use of V_j
                     w = mbar_wait(bar(L::kKvFull + vp.stage), vp.phase, ctx);
-                w = w && mbar_wait(bar(L::kPFull + t), p_phase[t], ctx);
-                p_phase[t] ^= 1u;
+                // The softmax releases P_t in two halves, so the tensor core
+                // starts on keys 0-63 while the exponentials of 64-127 run.
+                w = w && mbar_wait(bar(L::kPHalf + t), p_phase[t], ctx);
                 if (j == 0) w = w && mbar_wait(bar(L::kOEmpty + t), (ul & 1u) ^ 1u, ctx);
                 if (!__all_sync(0xffffffffu, w)) return false;
                 tc_fence_after_sync();  // P_t and the O_t rescale came from other threads' tcgen05.st
+                if (elect_one()) gemm_o(t, vp.stage, 0, j > 0);
+                __syncwarp();
+                w = mbar_wait(bar(L::kPFull + t), p_phase[t], ctx);
+                p_phase[t] ^= 1u;
+                if (!__all_sync(0xffffffffu, w)) return false;
+                tc_fence_after_sync();
                 if (elect_one()) {
-                    gemm_o(t, vp.stage, j > 0);
+                    gemm_o(t, vp.stage, 1, true);
                     if (t == 1) mma_commit(bar(L::kKvEmpty + vp.stage));  // V_j's last reader
                     if (j == ui.n[t] - 1) mma_commit(bar(L::kOFull + t));
                 }
@@ -340,44 +351,53 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 __syncwarp();
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after_sync();
+                // Load S_t in two halves: the second load is in flight while the
+                // first half is masked and reduced.
                 uint32_t r0[32], r1[32], r2[32], r3[32];
                 tmem_ld32(t_s + 0, r0);
                 tmem_ld32(t_s + 32, r1);
-                tmem_ld32(t_s + 64, r2);
-                tmem_ld32(t_s + 96, r3);
                 tmem_wait_ld(r0);
                 tmem_wait_ld(r1);
-                tmem_wait_ld(r2);
-                tmem_wait_ld(r3);
+                tmem_ld32(t_s + 64, r2);
+                tmem_ld32(t_s + 96, r3);
                 float* s0 = reinterpret_cast<float*>(r0);
                 float* s1 = reinterpret_cast<float*>(r1);
                 float* s2 = reinterpret_cast<float*>(r2);
                 float* s3 = reinterpret_cast<float*>(r3);
                 const int key0 = j * kBc;
                 const bool need_mask = (key0 + kBc > p.N) || (CAUSAL && j >= qt);
+                const int lim = CAUSAL ? min(p.N - 1, qrow) : p.N - 1;  // last visible key
                 if (need_mask) {
-                    const int lim = CAUSAL ? min(p.N - 1, qrow) : p.N - 1;  // last visible key
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         if (key0 + c > lim) s0[c] = -INFINITY;
                         if (key0 + 32 + c > lim) s1[c] = -INFINITY;
-                        if (key0 + 64 + c > lim) s2[c] = -INFINITY;
-                        if (key0 + 96 + c > lim) s3[c] = -INFINITY;
                     }
                 }
-                // row max: 3-input max over the 128 scores, four independent chains
+                // row max: 3-input max, two independent chains per half
                 float mx0 = fmax3(s0[0], s0[1], s0[2]), mx1 = fmax3(s1[0], s1[1], s1[2]);
-                float mx2 = fmax3(s2[0], s2[1], s2[2]), mx3 = fmax3(s3[0], s3[1], s3[2]);
 #pragma unroll
                 for (int c = 3; c < 31; c += 2) {
                     mx0 = fmax3(mx0, s0[c], s0[c + 1]);
                     mx1 = fmax3(mx1, s1[c], s1[c + 1]);
+                }
+                mx0 = fmax3(mx0, s0[31], fmaxf(mx1, s1[31]));
+                tmem_wait_ld(r2);
+                tmem_wait_ld(r3);
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        if (key0 + 64 + c > lim) s2[c] = -INFINITY;
+                        if (key0 + 96 + c > lim) s3[c] = -INFINITY;
+                    }
+                }
+                float mx2 = fmax3(s2[0], s2[1], s2[2]), mx3 = fmax3(s3[0], s3[1], s3[2]);
+#pragma unroll
+                for (int c = 3; c < 31; c += 2) {
                     mx2 = fmax3(mx2, s2[c], s2[c + 1]);
                     mx3 = fmax3(mx3, s3[c], s3[c + 1]);
                 }
-                mx0 = fmax3(mx0, s0[31], mx1);
-                mx2 = fmax3(mx2, s2[31], mx3);
-                mx0 = fmax3(mx0, s1[31], fmaxf(mx2, s3[31]));
+                mx0 = fmax3(mx0, fmax3(mx2, s2[31], mx3), s3[31]);
                 const float m_tile = mx0 * sl2;
                 const bool grow = m_tile > m_ref + kRescaleLog2;
                 float alpha = 1.f;
@@ -409,10 +429,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 };
                 exp_chunk(s0, 0);
                 exp_chunk(s1, 16);
-                exp_chunk(s2, 32);
-                exp_chunk(s3, 48);
-                l += (acc0 + acc1) + (acc2 + acc3);
-                // Rescale the O accumulator when this row's reference max moved.
+                // Rescale the O accumulator when this row's reference max moved,
+                // before the first half of P_t is released to O_t += P_t V.
                 // O_t's previous P V has completed: it was issued before this
                 // S_t, whose completion was just observed.
                 if (__any_sync(0xffffffffu, grow && j > 0)) {
@@ -426,6 +444,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         tmem_st32(t_o + c, o);
                     }
                 }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::kPHalf + t));
+                exp_chunk(s2, 32);
+                exp_chunk(s3, 48);
+                l += (acc0 + acc1) + (acc2 + acc3);
                 tmem_wait_st();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::kPFull + t));

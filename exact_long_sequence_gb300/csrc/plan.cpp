@@ -48,7 +48,7 @@ static Candidate evaluate(int N, int d, int causal, int q, int Bc) {
     const int q_bytes = q * kBr * d * 2;
     const int stage_bytes = Bc * d * 2;
     const int tmem = q * (Bc + d);
-    c.stages = (kSmemLimit - kSmemReserve - q_bytes) / stage_bytes;
+    c.stages = (kSmemLimit - overhead_bytes(0) - q_bytes) / (stage_bytes + 16);
     c.fits = tmem <= 512 && c.stages >= 3;
     c.l2_bytes = l2_traffic_per_head(N, d, q, causal);
     return c;

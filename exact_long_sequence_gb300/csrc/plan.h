@@ -17,20 +17,25 @@ constexpr int kQTiles = 2;        // query tiles per CTA, processed in ping-pong
 constexpr int kThreads = 384;     // warp 0 TMA, warp 1 MMA, warps 4-7 / 8-11 softmax of tile 0 / 1
 constexpr int kTmemCols = 512;    // S0 | S1 | O0 | O1 (P aliases the first half of S)
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per CTA on sm_100-family SMs
-constexpr int kSmemReserve = 1024 + 256;  // 1024-byte alignment slack + barriers and flags
+constexpr int kSmemAlign = 1024;    // slack to align the tiles to the 1024-byte swizzle atom
+constexpr int kFixedBarriers = 15;  // mbarriers besides the two per K/V stage
+constexpr int kFlagBytes = 16;      // TMEM base address slot and abort flag
 
 // Bytes of one [128 x d] bf16 tile (Q, K and V tiles all have this size since kBr == kBc).
 constexpr int tile_bytes(int d) { return kBr * d * 2; }
 
+// Bytes besides the tiles: alignment slack, mbarriers, flags.
+constexpr int overhead_bytes(int stages) { return kSmemAlign + (2 * stages + kFixedBarriers) * 8 + kFlagBytes; }
+
 // Deepest K/V ring that fits next to the resident query tiles, capped at 8.
 constexpr int kv_stages_for(int d) {
-    return ((kSmemLimit - kSmemReserve - kQTiles * tile_bytes(d)) / tile_bytes(d)) > 8
+    return ((kSmemLimit - overhead_bytes(0) - kQTiles * tile_bytes(d)) / (tile_bytes(d) + 16)) > 8
                ? 8
-               : ((kSmemLimit - kSmemReserve - kQTiles * tile_bytes(d)) / tile_bytes(d));
+               : ((kSmemLimit - overhead_bytes(0) - kQTiles * tile_bytes(d)) / (tile_bytes(d) + 16));
 }
 
 constexpr int smem_bytes_for(int d) {
-    return kSmemReserve + kQTiles * tile_bytes(d) + kv_stages_for(d) * tile_bytes(d);
+    return overhead_bytes(kv_stages_for(d)) + kQTiles * tile_bytes(d) + kv_stages_for(d) * tile_bytes(d);
 }
 
 static_assert(kv_stages_for(128) >= 3, "d=128 ring too shallow");
