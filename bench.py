@@ -332,7 +332,7 @@ def run_gb300(args, w):
         e2e = {"value": w.flops * len(e_ms) * world / e_slow / 1e12, "unit": UNIT,
                "ms_per_step": e_slow * 1e3 / len(e_ms),
                "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes + lse.numel() * 4,
-               "api": "attn_fwd_host (pinned host buffers, copies + kernel on one stream, wall clock)"}
+               "api": "attn_fwd_host (pinned host buffers; chunked copies overlapped with the kernels; wall clock until the caller's stream completes)"}
 
     if rank != 0:
         if world > 1:

@@ -180,6 +180,51 @@ extern "C" size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d) {
     return 4 * t + static_cast<size_t>(B) * H * N * 4;
 }
 
+namespace elsattn {
+namespace {
+
+// Streams and events of the host-buffer entry point, one set per device,
+// created on first use.  Copies in, kernels and copies out of consecutive
+// chunks of (batch, head) pairs run on separate streams so that the transfers
+// overlap the computation; two compute streams let one chunk's kernel start on
+// the SMs the previous chunk's kernel has finished with.
+constexpr int kMaxChunks = 8;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr, comp[2] = {nullptr, nullptr};
+    cudaEvent_t start = nullptr, done = nullptr, in[kMaxChunks] = {}, out[kMaxChunks] = {};
+};
+std::mutex g_pipe_mutex;
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(HostPipe** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    HostPipe& hp = g_pipe[dev];
+    if (!hp.ready) {
+        const unsigned f = cudaStreamNonBlocking;
+        if ((e = cudaStreamCreateWithFlags(&hp.h2d, f)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp.d2h, f)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp.comp[0], f)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&hp.comp[1], f)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e);
+        for (int c = 0; c < kMaxChunks; ++c)
+            if ((e = cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp.out[c], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e);
+        hp.ready = true;
+    }
+    *out = &hp;
+    return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace elsattn
+
 extern "C" int attn_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh, float* LSEh, int B, int H,
                              int N, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
                              cudaStream_t stream) {
@@ -190,17 +235,53 @@ extern "C" int attn_fwd_host(const void* Qh, const void* Kh, const void* Vh, voi
     const size_t bytes = static_cast<size_t>(B) * H * N * d * 2;
     const size_t t = (bytes + 255) & ~static_cast<size_t>(255);
     uint8_t* w = static_cast<uint8_t*>(workspace);
-    void *q = w, *k = w + t, *v = w + 2 * t, *o = w + 3 * t;
+    uint8_t *q = w, *k = w + t, *v = w + 2 * t, *o = w + 3 * t;
     float* lse = reinterpret_cast<float*>(w + 4 * t);
+    const uint8_t *qh = static_cast<const uint8_t*>(Qh), *kh = static_cast<const uint8_t*>(Kh),
+                  *vh = static_cast<const uint8_t*>(Vh);
+    uint8_t* oh = static_cast<uint8_t*>(Oh);
+
+    // Chunks of (batch, head) pairs: up to kMaxChunks of equal size.
+    const int BH = B * H;
+    const int chunks = BH < kMaxChunks ? BH : kMaxChunks;
+    const int per = (BH + chunks - 1) / chunks;
+    const size_t head_bytes = static_cast<size_t>(N) * d * 2;
+    const size_t head_lse = static_cast<size_t>(N);
+
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe* hp = nullptr;
+    if ((st = host_pipe(&hp)) != ATTN_OK) return st;
     cudaError_t e;
-    if ((e = cudaMemcpyAsync(q, Qh, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(k, Kh, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(v, Vh, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+    // Everything queued here runs after the work already on `stream`, and
+    // `stream` continues only after the last copy out.
+    if ((e = cudaEventRecord(hp->start, stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->h2d, hp->start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->d2h, hp->start, 0)) != cudaSuccess)
         return cuda_fail(e);
-    if ((st = attn_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream)) != ATTN_OK) return st;
-    if ((e = cudaMemcpyAsync(Oh, o, bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(LSEh, lse, static_cast<size_t>(B) * H * N * 4, cudaMemcpyDeviceToHost, stream)) !=
-            cudaSuccess)
+    int c = 0;
+    for (int h0 = 0; h0 < BH; h0 += per, ++c) {
+        const int hn = (BH - h0) < per ? (BH - h0) : per;
+        const size_t off = static_cast<size_t>(h0) * head_bytes, len = static_cast<size_t>(hn) * head_bytes;
+        const size_t loff = static_cast<size_t>(h0) * head_lse;
+        cudaStream_t comp = hp->comp[c & 1];
+        if ((e = cudaMemcpyAsync(q + off, qh + off, len, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(k + off, kh + off, len, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(v + off, vh + off, len, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
+            (e = cudaEventRecord(hp->in[c], hp->h2d)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(comp, hp->in[c], 0)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((st = attn_fwd(q + off, k + off, v + off, o + off, lse + loff, 1, hn, N, d, causal, scale, comp)) !=
+            ATTN_OK)
+            return st;
+        if ((e = cudaEventRecord(hp->out[c], comp)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hp->d2h, hp->out[c], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(oh + off, o + off, len, cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(LSEh + loff, lse + loff, static_cast<size_t>(hn) * head_lse * 4,
+                                 cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess)
+            return cuda_fail(e);
+    }
+    if ((e = cudaEventRecord(hp->done, hp->d2h)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, hp->done, 0)) != cudaSuccess)
         return cuda_fail(e);
     return ATTN_OK;
 }

@@ -88,9 +88,13 @@ int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, i
 
 /*
  * attn_fwd_host - the same operation on HOST buffers: copies Q, K, V to the
- * device, runs attn_fwd and copies O and LSE back, all queued on `stream`
- * (pinned host memory makes the copies asynchronous).  The caller synchronises
- * the stream before reading O / LSE.
+ * device, runs attn_fwd and copies O and LSE back.  The work is split into up
+ * to 8 chunks of (batch, head) pairs whose copies in, kernels and copies out
+ * run on the library's own per-device streams, so transfers overlap compute;
+ * it is ordered after the work already queued on `stream`, and `stream` waits
+ * for the last copy out.  Pinned host memory makes the copies asynchronous.
+ * The caller synchronises `stream` before reading O / LSE.  Calls from several
+ * host threads are serialised while they queue their work.
  *   Qh, Kh, Vh, Oh, LSEh : host pointers with the layouts of attn_fwd
  *   workspace            : device buffer of at least attn_fwd_host_workspace_bytes()
  *                          bytes, 16-byte aligned, owned by the caller

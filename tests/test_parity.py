@@ -149,6 +149,20 @@ def test_host_buffer_entry_matches_device_entry():
     assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
 
 
+@pytest.mark.parametrize("B,H,N,causal", [(2, 9, 333, True), (1, 1, 200, False), (3, 6, 1024, False)])
+def test_host_buffer_entry_chunks(oracle_mod, B, H, N, causal):
+    """The host-buffer entry splits (batch, head) pairs into chunks with overlapped
+    copies; results equal the oracle and the device entry for uneven chunk sizes."""
+    q, k, v = workloads.make_inputs(B, H, N, 64, seed=40 + N)
+    qp, kp, vp = (t.pin_memory() for t in (q, k, v))
+    o_h, l_h = ela.attn_fwd_host(qp, kp, vp, causal=causal)
+    torch.cuda.current_stream().synchronize()
+    compare(o_h, l_h, q, k, v, causal, ela.default_scale(64), None, oracle_mod, "host entry")
+    o_d, l_d = ela.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+
+
 def test_side_stream_and_scale(oracle_mod):
     q, k, v = workloads.make_inputs(2, 2, 200, 64, seed=11)
     s = torch.cuda.Stream()
