@@ -95,6 +95,25 @@ def test_more_units_than_sms(oracle_mod, causal):
     compare(o, lse, q, k, v, causal, ela.default_scale(64), None, oracle_mod, "many units")
 
 
+@pytest.mark.parametrize("N,d", [(1 << 20, 64), (1 << 19, 128)])
+def test_longest_sequences(oracle_mod, N, d):
+    """Million-token causal attention: sampled rows, always including the first and last."""
+    q, k, v = workloads.make_inputs(1, 1, N, d, seed=50 + d)
+    o, lse = run(q, k, v, True)
+    rows = workloads.sample_rows(1, N, 14, seed=50 + d)
+    rows = torch.cat([torch.tensor([[0, N - 1]]), rows], dim=1).sort(dim=1).values
+    compare(o, lse, q, k, v, True, ela.default_scale(d), rows, oracle_mod, f"N={N} d={d}")
+
+
+def test_many_heads(oracle_mod):
+    """16384 (batch, head) pairs of 64 tokens: every persistent CTA runs over a hundred units."""
+    B, H, N, d = 128, 128, 64, 64
+    q, k, v = workloads.make_inputs(B, H, N, d, seed=60)
+    o, lse = run(q, k, v, False)
+    rows = workloads.sample_rows(B * H, N, 3, seed=60)
+    compare(o, lse, q, k, v, False, ela.default_scale(d), rows, oracle_mod, "many heads")
+
+
 def test_outputs_stay_inside_their_buffers():
     """Guard canaries after O and LSE stay untouched."""
     B, H, N, d = 1, 2, 300, 128
