@@ -48,6 +48,13 @@ def _open(path: str):
         ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
     ]
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.oracle_attn_f64.restype = ctypes.c_int
+    lib.oracle_attn_f64.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 3 + [ctypes.c_int, ctypes.c_double,
+                                                                                     ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_attn_bwd_f64.restype = ctypes.c_int
+    lib.oracle_attn_bwd_f64.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3 + [ctypes.c_int, ctypes.c_double]
+                                        + [ctypes.c_void_p] * 3 + [ctypes.c_int])
     return lib
 
 
@@ -107,6 +114,48 @@ def attention_rows(q, k, v, causal: bool, scale: float, rows=None, nthreads: int
     return (O, LSE, P) if return_probs else (O, LSE)
 
 
+def _as_f64(x) -> np.ndarray:
+    """bf16 torch tensors are decoded exactly; float arrays are taken as given."""
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, dtype=np.float64)
+    import torch
+
+    return np.ascontiguousarray(x.detach().to("cpu").to(torch.float64).numpy())
+
+
+def attention_f64(q, k, v, causal: bool, scale: float, _lib_handle=None):
+    """Forward on double inputs, every row: (O [BH, N, d], LSE [BH, N])."""
+    qd, kd, vd = _as_f64(q), _as_f64(k), _as_f64(v)
+    N, d = qd.shape[-2], qd.shape[-1]
+    BH = int(np.prod(qd.shape[:-2]))
+    O = np.empty((BH, N, d))
+    LSE = np.empty((BH, N))
+    lib = _lib_handle if _lib_handle is not None else _load()
+    rc = lib.oracle_attn_f64(qd.ctypes.data, kd.ctypes.data, vd.ctypes.data, BH, N, d, int(bool(causal)),
+                             float(scale), O.ctypes.data, LSE.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_attn_f64 failed with status {rc}")
+    return O, LSE
+
+
+def attention_bwd(q, k, v, do, causal: bool, scale: float, nthreads: int | None = None, _lib_handle=None):
+    """Backward for upstream gradient dO: (dQ, dK, dV), each [BH, N, d] float64.
+    bf16 tensors are decoded exactly; float arrays are used as given."""
+    qd, kd, vd, dod = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
+    N, d = qd.shape[-2], qd.shape[-1]
+    BH = int(np.prod(qd.shape[:-2]))
+    dQ, dK, dV = (np.empty((BH, N, d)) for _ in range(3))
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    lib = _lib_handle if _lib_handle is not None else _load()
+    rc = lib.oracle_attn_bwd_f64(qd.ctypes.data, kd.ctypes.data, vd.ctypes.data, dod.ctypes.data, BH, N, d,
+                                 int(bool(causal)), float(scale), dQ.ctypes.data, dK.ctypes.data, dV.ctypes.data,
+                                 int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd_f64 failed with status {rc}")
+    return dQ, dK, dV
+
+
 class OracleBuild:
     """The same Python interface over another build of the C source (used by the
     mutation tests, which compile deliberately broken copies of the oracle)."""
@@ -116,3 +165,9 @@ class OracleBuild:
 
     def attention_rows(self, *args, **kwargs):
         return attention_rows(*args, _lib_handle=self._lib, **kwargs)
+
+    def attention_f64(self, *args, **kwargs):
+        return attention_f64(*args, _lib_handle=self._lib, **kwargs)
+
+    def attention_bwd(self, *args, **kwargs):
+        return attention_bwd(*args, _lib_handle=self._lib, **kwargs)

@@ -171,3 +171,171 @@ int oracle_attn_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
     free(tids);
     return status;
 }
+
+/* ------------------------------------------------------------------------
+ * Forward and backward on double-precision inputs.
+ *
+ * The backward pass is the derivative of the same attention graph with
+ * respect to Q, K and V for an upstream gradient dO of the output (the LSE is
+ * a saved statistic; no gradient flows into it).  With P the softmax
+ * probabilities of the scaled, masked scores and O = P V:
+ *     dV = P^T dO
+ *     dP = dO V^T
+ *     dS_ij = P_ij (dP_ij - D_i),  D_i = sum_k P_ik dP_ik = sum_c dO_ic O_ic
+ *     dQ = scale * dS K,   dK = scale * dS^T Q
+ * The "IO-Aware Algorithms" page describes FlashAttention's backward as
+ * recomputing these activations instead of storing them; the oracle simply
+ * computes them from the definition, one query row at a time.
+ * ------------------------------------------------------------------------ */
+
+/* The attention graph of one query row on double inputs (same steps as
+ * attend_one_row). */
+static void attend_one_row_f64(const double *q, const double *Kh, const double *Vh,
+                               int64_t N, int64_t d, int64_t i, int causal, double scale,
+                               double *s, double *o, double *lse)
+{
+    for (int64_t j = 0; j < N; ++j) {
+        const double *kj = Kh + j * d;
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            acc += q[c] * kj[c];
+        s[j] = scale * acc;
+    }
+    if (causal)
+        for (int64_t j = i + 1; j < N; ++j)
+            s[j] = -INFINITY;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < N; ++j)
+        if (s[j] > m) m = s[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        s[j] = exp(s[j] - m);
+        l += s[j];
+    }
+    for (int64_t j = 0; j < N; ++j)
+        s[j] /= l;
+    for (int64_t c = 0; c < d; ++c)
+        o[c] = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        if (s[j] == 0.0) continue;
+        const double *vj = Vh + j * d;
+        for (int64_t c = 0; c < d; ++c)
+            o[c] += s[j] * vj[c];
+    }
+    *lse = m + log(l);
+}
+
+/* Forward on double inputs: O [BH, N, d], LSE [BH, N] for every row. */
+int oracle_attn_f64(const double *Q, const double *K, const double *V, int64_t BH, int64_t N, int64_t d,
+                    int causal, double scale, double *O, double *LSE)
+{
+    if (!Q || !K || !V || !O || !LSE || BH < 0 || N < 1 || d < 1) return 1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!s) return 2;
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        const int64_t head = bh * N * d;
+        for (int64_t i = 0; i < N; ++i)
+            attend_one_row_f64(Q + head + i * d, K + head, V + head, N, d, i, causal, scale, s,
+                               O + head + i * d, LSE + bh * N + i);
+    }
+    free(s);
+    return 0;
+}
+
+typedef struct {
+    const double *Q, *K, *V, *dO; /* one head, [N, d] */
+    int64_t N, d, first, last;    /* query rows [first, last) */
+    int causal;
+    double scale;
+    double *dQ;                   /* [N, d], rows [first, last) written */
+    double *dK, *dV;              /* [N, d] partial sums of this worker */
+    int status;
+} bwd_job;
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *jb = (bwd_job *)arg;
+    const int64_t N = jb->N, d = jb->d;
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    double *o = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!p || !o) { free(p); free(o); jb->status = 2; return NULL; }
+    for (int64_t i = jb->first; i < jb->last; ++i) {
+        const double *qi = jb->Q + i * d, *doi = jb->dO + i * d;
+        double lse;
+        attend_one_row_f64(qi, jb->K, jb->V, N, d, i, jb->causal, jb->scale, p, o, &lse);
+        double Di = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            Di += doi[c] * o[c];
+        double *dqi = jb->dQ + i * d;
+        for (int64_t c = 0; c < d; ++c)
+            dqi[c] = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            if (p[j] == 0.0) continue;
+            const double *vj = jb->V + j * d, *kj = jb->K + j * d;
+            double dPij = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                dPij += doi[c] * vj[c];
+            const double dSij = p[j] * (dPij - Di);
+            double *dkj = jb->dK + j * d, *dvj = jb->dV + j * d;
+            for (int64_t c = 0; c < d; ++c) {
+                dqi[c] += jb->scale * dSij * kj[c];
+                dkj[c] += jb->scale * dSij * qi[c];
+                dvj[c] += p[j] * doi[c];
+            }
+        }
+    }
+    free(p);
+    free(o);
+    return NULL;
+}
+
+/* Backward on double inputs for BH independent heads: dQ, dK, dV [BH, N, d]. */
+int oracle_attn_bwd_f64(const double *Q, const double *K, const double *V, const double *dO, int64_t BH,
+                        int64_t N, int64_t d, int causal, double scale, double *dQ, double *dK, double *dV,
+                        int nthreads)
+{
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV || BH < 0 || N < 1 || d < 1) return 1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > N) nthreads = (int)N;
+    const size_t head_elems = (size_t)N * (size_t)d;
+    double *part = (double *)calloc((size_t)nthreads * 2 * head_elems, sizeof(double));
+    bwd_job *jobs = (bwd_job *)calloc((size_t)nthreads, sizeof(bwd_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!part || !jobs || !tids) { free(part); free(jobs); free(tids); return 2; }
+    int status = 0;
+    for (int64_t bh = 0; bh < BH && !status; ++bh) {
+        const size_t off = (size_t)bh * head_elems;
+        memset(part, 0, (size_t)nthreads * 2 * head_elems * sizeof(double));
+        for (int t = 0; t < nthreads; ++t) {
+            bwd_job jb = {Q + off, K + off, V + off, dO + off, N, d, N * t / nthreads, N * (t + 1) / nthreads,
+                          causal, scale, dQ + off, part + (size_t)(2 * t) * head_elems,
+                          part + (size_t)(2 * t + 1) * head_elems, 0};
+            jobs[t] = jb;
+        }
+        int started = 0;
+        for (int t = 1; t < nthreads; ++t) {
+            if (pthread_create(&tids[t], NULL, bwd_worker, &jobs[t]) != 0) break;
+            started = t;
+        }
+        bwd_worker(&jobs[0]);
+        for (int t = started + 1; t < nthreads; ++t)
+            bwd_worker(&jobs[t]);
+        for (int t = 1; t <= started; ++t)
+            pthread_join(tids[t], NULL);
+        for (int t = 0; t < nthreads; ++t)
+            if (jobs[t].status) status = jobs[t].status;
+        for (size_t e = 0; e < head_elems; ++e) {
+            double sk = 0.0, sv = 0.0;
+            for (int t = 0; t < nthreads; ++t) {
+                sk += part[(size_t)(2 * t) * head_elems + e];
+                sv += part[(size_t)(2 * t + 1) * head_elems + e];
+            }
+            dK[off + e] = sk;
+            dV[off + e] = sv;
+        }
+    }
+    free(part);
+    free(jobs);
+    free(tids);
+    return status;
+}
