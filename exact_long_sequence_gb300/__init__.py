@@ -42,6 +42,8 @@ EXPORTED_SYMBOLS = (
     "attn_strerror",
     "attn_debug_wait_timeout",
     "attn_fwd_noalloc",
+    "attn_bwd",
+    "attn_bwd_workspace_bytes",
 )
 
 
@@ -101,6 +103,10 @@ def load_library(path: str | None = None):
     lib.attn_debug_wait_timeout.restype = i
     lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.attn_fwd_noalloc.restype = i
+    lib.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+    lib.attn_bwd.restype = i
+    lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
     if path is None:
         _lib = lib
     return lib
@@ -156,6 +162,35 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
                           B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
     _check(st, "attn_fwd")
     return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, workspace=None, stream=None):
+    """dQ, dK, dV = gradients of attn_fwd for the upstream gradient `do`.
+
+    q, k, v, o, do : bf16 CUDA tensors [B, H, N, d] (o, lse from attn_fwd on the same inputs)
+    lse            : fp32 [B, H, N]
+    """
+    import torch
+
+    lib = load_library()
+    for t in (q, k, v, o, do):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v, o, do must be contiguous bf16 CUDA tensors of one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    if scale is None:
+        scale = default_scale(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    need = lib.attn_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                          workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_noalloc(q, k, v, out, lse, causal: bool = False, scale: float | None = None, stream=None):

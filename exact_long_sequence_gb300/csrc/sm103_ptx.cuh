@@ -70,19 +70,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking test of whether the phase with the given parity has completed.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Wait for the phase with the given parity to complete.  Returns false if the
 // CTA was aborted by another role or if the time limit ran out (in which case
 // this call records the timeout and aborts the CTA).
@@ -243,6 +230,18 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  : ELS_U8(0), ELS_U8(8), ELS_U8(16), ELS_U8(24)
                  :
                  : "memory");
+}
+
+// 16-column variants.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : ELS_R8(0), ELS_R8(8)
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : ELS_U8(0), ELS_U8(8) : : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {

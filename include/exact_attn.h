@@ -106,6 +106,32 @@ int attn_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh, floa
 size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * attn_bwd - gradients of attn_fwd for an upstream gradient dO of O:
+ *     dV = P^T dO,  dS = P * (dO V^T - D) with D_i = sum_c dO_ic O_ic,
+ *     dQ = scale * dS K,  dK = scale * dS^T Q,
+ * where P = softmax(scale * Q K^T + mask) is recomputed from Q, K and the
+ * forward's LSE instead of being stored (FlashAttention's recomputation in the
+ * backward pass, "IO-Aware Algorithms").  No gradient flows into LSE.
+ *   Q, K, V, O, dO : const bf16 [B,H,N,d] device pointers (O and LSE as written
+ *                    by attn_fwd for the same Q, K, V, causal, scale)
+ *   LSE            : const fp32 [B,H,N]
+ *   dQ, dK, dV     : bf16 [B,H,N,d] device pointers (written)
+ *   workspace      : device buffer of at least attn_bwd_workspace_bytes() bytes,
+ *                    16-byte aligned, owned by the caller: the fp32 dQ accumulator
+ *                    [B,H,N,d], then D and LSE * log2(e) on rows padded to a
+ *                    multiple of 128 per (batch, head)
+ * Same size, alignment and error rules as attn_fwd; asynchronous on `stream`.
+ */
+int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
+             void* dK, void* dV, int B, int H, int N, int d, int causal, float scale, void* workspace,
+             size_t workspace_bytes, cudaStream_t stream);
+
+/* Device bytes attn_bwd needs as workspace:
+ * align256(4*B*H*N*d) + 2 * align256(4*B*H*ceil(N/128)*128); 0 for a
+ * non-positive size. */
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * attn_plan - host only, launches nothing.  Fills *out with the tiling the
  * planner derives from an I/O count of the two tall-and-skinny products
  * (S = Q K^T and O = P V) against the shared- and tensor-memory capacity of an

@@ -112,3 +112,20 @@ def test_zero_upstream_gradient(oracle_mod):
     q, k, v = (rnd((1, 20, 8), s) for s in (21, 22, 23))
     for g in oracle_mod.attention_bwd(q, k, v, np.zeros_like(q), True, 0.3):
         assert (g == 0).all()
+
+
+def test_single_visible_key_has_no_score_gradient(oracle_mod):
+    """A query that sees one key has P = 1 whatever its score, so its score gradient is 0:
+    with N = 1, dQ = dK = 0 and dV = dO; with the causal mask, query 0 sees only key 0,
+    so dQ_0 = 0, and the last key is seen only by the last query: dV_{N-1} = P_{N-1,N-1} dO_{N-1}."""
+    q, k, v, do = (rnd((1, 1, 6), s) for s in (24, 25, 26, 27))
+    dQ, dK, dV = oracle_mod.attention_bwd(q, k, v, do, False, 0.4)
+    assert (dQ == 0).all() and (dK == 0).all()
+    np.testing.assert_array_equal(dV[0], do[0])
+    N, d, scale = 9, 5, 0.45
+    q, k, v, do = (rnd((1, N, d), s) for s in (28, 29, 30, 31))
+    dQ, dK, dV = oracle_mod.attention_bwd(q, k, v, do, True, scale)
+    assert (dQ[0, 0] == 0).all()
+    s = scale * q[0, -1] @ k[0].T
+    p_last = math.exp(s[-1] - s.max()) / np.exp(s - s.max()).sum()
+    np.testing.assert_allclose(dV[0, -1], p_last * do[0, -1], rtol=1e-13)
