@@ -11,17 +11,13 @@
 #include <mutex>
 
 #include "../../include/exact_attn.h"
-#include "attn_bwd_kernel.cuh"
+#include "api_common.h"
 #include "attn_fwd_kernel.cuh"
 #include "plan.h"
 
 extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out);
 
 namespace elsattn {
-namespace {
-
-constexpr int kMaxDevices = 64;
-constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s for any single wait
 
 thread_local int g_last_cuda_error = 0;
 
@@ -30,17 +26,11 @@ int cuda_fail(cudaError_t e) {
     return ATTN_ERR_CUDA;
 }
 
-struct DeviceState {
-    bool ready = false;
-    int num_sms = 0;
-    int cc_major = 0, cc_minor = 0;
-    uint32_t* error_word = nullptr;  // 256-byte device block, first word = error code
-    bool smem_configured[2][2] = {{false, false}, {false, false}};
-};
-
+namespace {
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+}  // namespace
 
 int device_state(DeviceState** out) {
     int dev = 0;
@@ -77,13 +67,10 @@ int device_state(DeviceState** out) {
     return ATTN_OK;
 }
 
-// Q, K, V viewed as a 3-D tensor [BH][N][d] (d innermost), read in boxes of
-// 64 columns x 128 rows with the 128-byte swizzle the tcgen05 descriptors
-// expect.  Rows past N read as zero.
-int encode_qkv_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+int encode_rows_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBr), 1};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -105,6 +92,8 @@ int check_args(const void* Q, const void* K, const void* V, const void* O, const
     if ((reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return ATTN_ERR_MISALIGNED;
     return ATTN_OK;
 }
+
+namespace {
 
 template <int D, bool CAUSAL>
 int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, const CUtensorMap& tk,
@@ -149,8 +138,8 @@ extern "C" int attn_fwd(const void* Q, const void* K, const void* V, void* O, fl
 
     const int BH = B * H;
     CUtensorMap tq, tk, tv;
-    if ((st = encode_qkv_map(&tq, Q, BH, N, d)) != ATTN_OK || (st = encode_qkv_map(&tk, K, BH, N, d)) != ATTN_OK ||
-        (st = encode_qkv_map(&tv, V, BH, N, d)) != ATTN_OK)
+    if ((st = encode_rows_map(&tq, Q, BH, N, d, kBr)) != ATTN_OK || (st = encode_rows_map(&tk, K, BH, N, d, kBc)) != ATTN_OK ||
+        (st = encode_rows_map(&tv, V, BH, N, d, kBc)) != ATTN_OK)
         return st;
 
     FwdParams p;
@@ -285,107 +274,6 @@ extern "C" int attn_fwd_host(const void* Qh, const void* Kh, const void* Vh, voi
         (e = cudaStreamWaitEvent(stream, hp->done, 0)) != cudaSuccess)
         return cuda_fail(e);
     return ATTN_OK;
-}
-
-// ----------------------------------------------------------------- backward
-namespace elsattn {
-namespace {
-
-template <int D, bool CAUSAL>
-int launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-               const BwdParams& p, int BH, cudaStream_t stream) {
-    static bool configured[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    auto kernel = attn_bwd_kernel<D, CAUSAL>;
-    if (!configured[dev]) {
-        if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdLayout<D>::kSmem)) !=
-            cudaSuccess)
-            return cuda_fail(e);
-        configured[dev] = true;
-    }
-    kernel<<<BH * p.num_q_tiles, kBwdThreads, BwdLayout<D>::kSmem, stream>>>(tq, tk, tv, tdo, p);
-    e = cudaGetLastError();
-    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
-}
-
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-
-}  // namespace
-}  // namespace elsattn
-
-extern "C" size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
-    if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
-    const size_t rows = static_cast<size_t>(B) * H * N;
-    const size_t padded = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + kBr - 1) / kBr * kBr);
-    return align256(rows * d * 4) + 2 * align256(padded * 4);
-}
-
-extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
-                        void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
-                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    int st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
-    if (st != ATTN_OK) return st;
-    if (!dO || !dQ || !dK || !dV || !workspace) return ATTN_ERR_INVALID_ARG;
-    if (!aligned16(dO) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV) || !aligned16(workspace))
-        return ATTN_ERR_MISALIGNED;
-    if (workspace_bytes < attn_bwd_workspace_bytes(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
-    DeviceState* dev = nullptr;
-    if ((st = device_state(&dev)) != ATTN_OK) return st;
-
-    const int BH = B * H;
-    const size_t rows = static_cast<size_t>(BH) * N;
-    const int nq = (N + kBr - 1) / kBr;
-    const int Np = nq * kBr;
-    const size_t padded = static_cast<size_t>(BH) * Np;
-    float* dqacc = static_cast<float*>(workspace);
-    float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * d * 4));
-    float* lse2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dvec) + align256(padded * 4));
-    CUtensorMap tq, tk, tv, tdo;
-    if ((st = encode_qkv_map(&tq, Q, BH, N, d)) != ATTN_OK || (st = encode_qkv_map(&tk, K, BH, N, d)) != ATTN_OK ||
-        (st = encode_qkv_map(&tv, V, BH, N, d)) != ATTN_OK || (st = encode_qkv_map(&tdo, dO, BH, N, d)) != ATTN_OK)
-        return st;
-
-    // D_i = sum_c dO_ic O_ic and LSE_i * log2(e) on tile-padded rows; the dQ accumulator zeroed
-    {
-        const size_t threads = padded * (d / 8);
-        const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-        const auto* o = static_cast<const __nv_bfloat16*>(O);
-        const auto* g = static_cast<const __nv_bfloat16*>(dO);
-        if (d == 64)
-            attn_bwd_prep_kernel<64><<<blocks, 256, 0, stream>>>(o, g, LSE, dvec, lse2, dqacc, N, Np, padded);
-        else
-            attn_bwd_prep_kernel<128><<<blocks, 256, 0, stream>>>(o, g, LSE, dvec, lse2, dqacc, N, Np, padded);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail(e);
-    }
-    BwdParams p;
-    p.dQacc = dqacc;
-    p.lse2 = lse2;
-    p.Dvec = dvec;
-    p.dK = static_cast<__nv_bfloat16*>(dK);
-    p.dV = static_cast<__nv_bfloat16*>(dV);
-    p.error_word = dev->error_word;
-    p.timeout_ns = kDefaultTimeoutNs;
-    p.N = N;
-    p.num_q_tiles = nq;
-    p.Np = Np;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.scale = scale;
-    if (d == 64)
-        st = causal ? launch_bwd<64, true>(tq, tk, tv, tdo, p, BH, stream)
-                    : launch_bwd<64, false>(tq, tk, tv, tdo, p, BH, stream);
-    else
-        st = causal ? launch_bwd<128, true>(tq, tk, tv, tdo, p, BH, stream)
-                    : launch_bwd<128, false>(tq, tk, tv, tdo, p, BH, stream);
-    if (st != ATTN_OK) return st;
-    // dQ = bf16(accumulator)
-    const size_t n4 = rows * d / 4;
-    attn_bwd_post_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(
-        dqacc, static_cast<__nv_bfloat16*>(dQ), n4);
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
 extern "C" int attn_last_device_error(cudaStream_t stream) {
@@ -534,8 +422,8 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, voi
 
     const int BH = B * H;
     CUtensorMap tq, tk, tv;
-    if ((st = encode_qkv_map(&tq, Q, BH, N, d)) != ATTN_OK || (st = encode_qkv_map(&tk, K, BH, N, d)) != ATTN_OK ||
-        (st = encode_qkv_map(&tv, V, BH, N, d)) != ATTN_OK)
+    if ((st = encode_rows_map(&tq, Q, BH, N, d, kBr)) != ATTN_OK || (st = encode_rows_map(&tk, K, BH, N, d, kBc)) != ATTN_OK ||
+        (st = encode_rows_map(&tv, V, BH, N, d, kBc)) != ATTN_OK)
         return st;
 
     // The array keeps the previous call's contents: the error word must start at zero.

@@ -4,25 +4,32 @@
 // The "IO-Aware Algorithms" page notes that FlashAttention recomputes its
 // activations in the backward pass instead of storing them; this kernel does
 // the same: it never stores P.  With the forward's per-row log-sum-exp it
-// recomputes P = exp(scale * q.k - LSE) tile by tile and applies
+// recomputes P = exp(scale * q.k - LSE) block by block and applies
 //     dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D)  (D_i = sum_c dO_ic O_ic),
 //     dQ = scale * dS K,  dK = scale * dS^T Q.
 //
 // One CTA owns one (batch, head) and one tile of 128 keys; K_j and V_j stay in
-// shared memory while the query tiles Q_i, dO_i stream through a TMA ring.
-// Per query tile the MMA warp issues, all on tcgen05 with fp32 accumulators in
-// TMEM (the key index is the MMA's M dimension, one TMEM lane per key):
-//     S^T  = K_j Q_i^T           (A = K_j, B = Q_i, both from shared memory)
-//     dP^T = V_j dO_i^T          (A = V_j, B = dO_i)
-//     dV  += P^T dO_i            (A = P^T bf16 in TMEM, B = dO_i)
-//     dK  += dS^T Q_i            (A = dS^T bf16 in TMEM, B = Q_i)
-//     dQ_i = dS K_j              (A = dS bf16 in shared memory, M = queries)
-// The compute warpgroup (thread r = key row r) turns S^T into P^T and dP^T
-// into dS^T (scale folded in), writes dS^T to TMEM and dS to shared memory,
-// and adds the partial dQ_i into an fp32 accumulator in global memory.
+// shared memory while blocks of 64 queries (Q_i, dO_i) stream through a TMA
+// ring.  Per query block the MMA warp issues, on tcgen05 with fp32
+// accumulators in TMEM:
+//     S^T  = K_j Q_i^T     M = 128 keys, N = 64 queries   (A, B in shared memory)
+//     dP^T = V_j dO_i^T    M = 128 keys, N = 64 queries
+//     dV  += P^T dO_i      M = 128 keys, N = d            (A = P^T bf16 in TMEM)
+//     dK  += dS^T Q_i      M = 128 keys, N = d            (A = dS^T bf16 in TMEM)
+//     dQ_i^T = K_j^T dS^T  M = d (padded to 128), N = 64  (A = K_j read transposed)
+// S^T and dP^T are double-buffered in TMEM, so the tensor core computes the
+// scores of block i+2 while the compute warps still work on block i.  dQ is
+// produced transposed so that TMEM lane = head-dim column: the readout warps
+// then add it to the fp32 accumulator with one full 128-byte line per warp
+// instruction, and they release the TMEM columns before issuing the adds.
 //
-// TMEM columns: [0,128) S^T, then P^T (first 64), then the dQ_i partial |
-// [128,256) dP^T, then dS^T (first 64) | [256,256+d) dV | [256+d,256+2d) dK.
+// Warp roles: 0 TMA producer, 1 MMA issuer, 4-7 P and dS (thread = key row),
+// 8-11 dQ readout (thread = head-dim column); at the end 4-7 write dV and
+// 8-11 write dK.
+//
+// TMEM columns: [0, d) dV | [d, 2d) dK | buffer b at 2d + 128 b:
+//   [0, 64) S^T, P^T (bf16) over its first 32;  [64, 128) dP^T, dS^T (bf16)
+//   over its first 32, then dQ^T of the block (fp32).
 #pragma once
 
 #include <cuda.h>
@@ -33,8 +40,9 @@
 
 namespace elsattn {
 
-constexpr int kBwdThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 4-7 compute
-constexpr int kBwdStages = 2;     // Q_i + dO_i ring depth
+constexpr int kBwdThreads = 384;  // warps 0 TMA, 1 MMA, 4-7 P/dS, 8-11 dQ readout
+constexpr int kBq = 64;           // queries per block
+constexpr int kBwdStages = 4;     // Q_i + dO_i ring depth
 
 struct BwdParams {
     float* dQacc;          // [BH, N, d] fp32, zeroed; receives scale * dS K
@@ -45,38 +53,46 @@ struct BwdParams {
     uint32_t* error_word;
     uint64_t timeout_ns;
     int N;
-    int num_q_tiles;       // ceil(N / 128)
-    int Np;                // num_q_tiles * 128: row stride of lse2 and Dvec
+    int num_k_tiles;       // ceil(N / 128): CTAs per (batch, head)
+    int num_q_blocks;      // ceil(N / 64)
+    int Np;                // num_k_tiles * 128: row stride of lse2 and Dvec
     float scale_log2;      // scale * log2(e)
     float scale;
 };
 
 template <int D>
 struct BwdLayout {
-    static constexpr int kTile = tile_bytes(D);          // one [128 x d] bf16 tile
+    static constexpr int kKvTile = 128 * D * 2;             // K_j or V_j: [128 keys x d] bf16
+    static constexpr int kQTile = kBq * D * 2;              // Q_i or dO_i: [64 queries x d] bf16
+    static constexpr int kKvBlock = 128 * 128;              // one 64-column block of a K/V tile
+    static constexpr int kQBlock = kBq * 128;               // one 64-column block of a Q/dO tile
     static constexpr int kKOff = 0;
-    static constexpr int kVOff = kTile;
-    static constexpr int kRingOff = 2 * kTile;            // stage s: Q_i at +0, dO_i at +kTile
-    static constexpr int kDsOff = kRingOff + kBwdStages * 2 * kTile;  // dS, [2 query blocks][128 keys][64]
-    static constexpr int kDsBytes = 2 * 128 * 128;
-    static constexpr int kBarOff = kDsOff + kDsBytes;
+    static constexpr int kVOff = kKvTile;
+    static constexpr int kRingOff = 2 * kKvTile;            // stage s: Q_i at +0, dO_i at +kQTile
+    static constexpr int kStageBytes = 2 * kQTile;
+    static constexpr int kDsOff = kRingOff + kBwdStages * kStageBytes;  // [2][128 keys][64 queries] bf16
+    static constexpr int kDsBuf = 128 * kBq * 2;
+    static constexpr int kBarOff = kDsOff + 2 * kDsBuf;
     // barriers
     static constexpr int kKvFull = 0;
-    static constexpr int kQFull = 1;                      // [kBwdStages]
-    static constexpr int kQEmpty = kQFull + kBwdStages;   // [kBwdStages]
-    static constexpr int kSpFull = kQEmpty + kBwdStages;  // S^T and dP^T complete
-    static constexpr int kPFull = kSpFull + 1;            // P^T in TMEM (4 warp arrivals)
-    static constexpr int kDsFull = kPFull + 1;            // dS^T in TMEM, dS in shared memory (4)
-    static constexpr int kDsEmpty = kDsFull + 1;          // dQ_i MMA done reading dS
-    static constexpr int kDqFull = kDsEmpty + 1;          // dQ_i partial complete
-    static constexpr int kStFree = kDqFull + 1;           // dQ_i partial read out (4)
-    static constexpr int kKvDone = kStFree + 1;           // dK, dV accumulation complete
+    static constexpr int kQFull = 1;                         // [kBwdStages]
+    static constexpr int kQEmpty = kQFull + kBwdStages;      // [kBwdStages]
+    static constexpr int kSpFull = kQEmpty + kBwdStages;     // [2] S^T and dP^T of a block complete
+    static constexpr int kPFull = kSpFull + 2;               // [2] P^T in TMEM (4 warp arrivals)
+    static constexpr int kDsFull = kPFull + 2;               // [2] dS^T in TMEM, dS in shared memory (4)
+    static constexpr int kDsEmpty = kDsFull + 2;             // [2] dQ^T MMA done reading dS
+    static constexpr int kDqFull = kDsEmpty + 2;             // [2] dQ^T of a block complete
+    static constexpr int kDqFree = kDqFull + 2;              // [2] dQ^T read out of TMEM (4)
+    static constexpr int kKvDone = kDqFree + 2;              // dK, dV accumulation complete
     static constexpr int kDrain = kKvDone + 1;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr int kFlagsOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kFlagsOff + 16;
     static constexpr int kSmem = kBytes + kSmemAlign;
     static_assert(kSmem <= kSmemLimit, "backward shared memory");
+    static_assert(2 * kSmem > 233472, "one CTA per SM: each allocates all TMEM columns");
+    static_assert(kRingOff % 1024 == 0 && kStageBytes % 1024 == 0 && kQTile % 1024 == 0 && kDsOff % 1024 == 0,
+                  "swizzle atoms are 1024-byte aligned");
 };
 
 template <int D, bool CAUSAL>
@@ -96,10 +112,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const int lane = threadIdx.x & 31;
     const WaitCtx ctx{abort_flag, p.error_word, p.timeout_ns};
 
-    const int bh = blockIdx.x / p.num_q_tiles;     // key tiles per head == query tiles per head
-    const int kt = blockIdx.x - bh * p.num_q_tiles;
-    const int i_first = CAUSAL ? kt : 0;           // query tiles before the key tile see none of its keys
-    const int n_iter = p.num_q_tiles - i_first;
+    const int bh = blockIdx.x / p.num_k_tiles;
+    const int kt = blockIdx.x - bh * p.num_k_tiles;
+    const int i_first = CAUSAL ? 2 * kt : 0;     // query blocks before the key tile see none of its keys
+    const int n_iter = p.num_q_blocks - i_first;  // >= 1: the diagonal block is always visited
 
     if (threadIdx.x == 0) {
         *abort_flag = 0u;
@@ -108,12 +124,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             mbar_init(bar(L::kQFull + s), 1);
             mbar_init(bar(L::kQEmpty + s), 1);
         }
-        mbar_init(bar(L::kSpFull), 1);
-        mbar_init(bar(L::kPFull), 4);
-        mbar_init(bar(L::kDsFull), 4);
-        mbar_init(bar(L::kDsEmpty), 1);
-        mbar_init(bar(L::kDqFull), 1);
-        mbar_init(bar(L::kStFree), 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::kSpFull + b), 1);
+            mbar_init(bar(L::kPFull + b), 4);
+            mbar_init(bar(L::kDsFull + b), 4);
+            mbar_init(bar(L::kDsEmpty + b), 1);
+            mbar_init(bar(L::kDqFull + b), 1);
+            mbar_init(bar(L::kDqFree + b), 4);
+        }
         mbar_init(bar(L::kKvDone), 1);
         mbar_init(bar(L::kDrain), 1);
         fence_barrier_init();
@@ -130,24 +148,24 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer
         bool ok = true;
-        mbar_arrive_expect_tx(bar(L::kKvFull), 2 * L::kTile);
+        mbar_arrive_expect_tx(bar(L::kKvFull), 2 * L::kKvTile);
 #pragma unroll
         for (int b = 0; b < D / 64; ++b) {
-            tma_load_3d(s_base + L::kKOff + b * 16384, &tmap_k, bar(L::kKvFull), b * 64, kt * kBc, bh);
-            tma_load_3d(s_base + L::kVOff + b * 16384, &tmap_v, bar(L::kKvFull), b * 64, kt * kBc, bh);
+            tma_load_3d(s_base + L::kKOff + b * L::kKvBlock, &tmap_k, bar(L::kKvFull), b * 64, kt * kBc, bh);
+            tma_load_3d(s_base + L::kVOff + b * L::kKvBlock, &tmap_v, bar(L::kKvFull), b * 64, kt * kBc, bh);
         }
         int issued = 0;
         for (int it = 0; it < n_iter && ok; ++it) {
             const int s = it % kBwdStages;
             ok = mbar_wait(bar(L::kQEmpty + s), ((it / kBwdStages) & 1) ^ 1, ctx);
             if (!ok) break;
-            mbar_arrive_expect_tx(bar(L::kQFull + s), 2 * L::kTile);
-            const uint32_t dst = s_base + L::kRingOff + s * 2 * L::kTile;
-            const int row = (i_first + it) * kBr;
+            mbar_arrive_expect_tx(bar(L::kQFull + s), L::kStageBytes);
+            const uint32_t dst = s_base + L::kRingOff + s * L::kStageBytes;
+            const int row = (i_first + it) * kBq;
 #pragma unroll
             for (int b = 0; b < D / 64; ++b) {
-                tma_load_3d(dst + b * 16384, &tmap_q, bar(L::kQFull + s), b * 64, row, bh);
-                tma_load_3d(dst + L::kTile + b * 16384, &tmap_do, bar(L::kQFull + s), b * 64, row, bh);
+                tma_load_3d(dst + b * L::kQBlock, &tmap_q, bar(L::kQFull + s), b * 64, row, bh);
+                tma_load_3d(dst + L::kQTile + b * L::kQBlock, &tmap_do, bar(L::kQFull + s), b * 64, row, bh);
             }
             issued = it + 1;
         }
@@ -157,101 +175,121 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             mbar_wait_drain(bar(L::kQFull + it % kBwdStages), (it / kBwdStages) & 1, 50000000ull);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t id_nt = make_idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-        constexpr uint32_t id_tn = make_idesc_bf16_f32(128, D, false, true);      // dV, dK (A in TMEM)
-        constexpr uint32_t id_mn = make_idesc_bf16_f32(128, D, true, true);       // dQ (A MN-major)
-        const uint32_t t_st = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
-        const uint64_t dk_k = make_smem_desc_sw128(s_base + L::kKOff, 16, 1024);      // K_j, K-major
-        const uint64_t dv_k = make_smem_desc_sw128(s_base + L::kVOff, 16, 1024);      // V_j, K-major
-        const uint64_t dk_mn = make_smem_desc_sw128(s_base + L::kKOff, 16384, 1024);  // K_j, MN-major
-        const uint64_t dds_mn = make_smem_desc_sw128(s_base + L::kDsOff, 16384, 1024);  // dS, MN-major
+        constexpr uint32_t id_s = make_idesc_bf16_f32(128, kBq, false, false);  // S^T, dP^T
+        constexpr uint32_t id_acc = make_idesc_bf16_f32(128, D, false, true);   // dV, dK (A in TMEM)
+        constexpr uint32_t id_dq = make_idesc_bf16_f32(128, kBq, true, true);   // dQ^T (A, B MN-major)
+        const uint32_t t_dv = tmem, t_dk = tmem + D;
+        const uint64_t dk_k = make_smem_desc_sw128(s_base + L::kKOff, 16, 1024);            // K_j, K-major
+        const uint64_t dv_k = make_smem_desc_sw128(s_base + L::kVOff, 16, 1024);            // V_j, K-major
+        // K_j^T as A of dQ^T: d-blocks of 64 are L::kKvBlock apart.  For d = 64 the
+        // second block (rows 64..127 of dQ^T) reads V_j: those lanes are never used.
+        const uint64_t dkt_mn = make_smem_desc_sw128(s_base + L::kKOff, L::kKvBlock, 1024);
+        auto ring = [&](int i) { return s_base + L::kRingOff + static_cast<uint32_t>(i % kBwdStages) * L::kStageBytes; };
+        auto kstep_a = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * L::kKvBlock + (kk & 3) * 32) >> 4); };
+        auto kstep_b = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * L::kQBlock + (kk & 3) * 32) >> 4); };
+        constexpr uint64_t kRows16 = (16 * 128) >> 4;  // 16 rows of an MN-major operand
+
+        // S^T and dP^T of block i into buffer i & 1.  The S^T half is free: P^T of
+        // block i - 2 was read by dV (issued earlier) and by the dS pass (its
+        // DsFull was awaited).  The dP^T half holds dQ^T of block i - 2 until the
+        // readout warps release it.
+        auto issue_sdp = [&](int i) -> bool {
+            const int b = i & 1;
+            const uint32_t q = ring(i);
+            bool w = mbar_wait(bar(L::kQFull + i % kBwdStages), (i / kBwdStages) & 1, ctx);
+            if (!__all_sync(0xffffffffu, w)) return false;
+            tc_fence_after_sync();
+            const uint32_t t_s = tmem + 2 * D + 128 * b;
+            const uint64_t dq_k = make_smem_desc_sw128(q, 16, 1024);
+            const uint64_t ddo_k = make_smem_desc_sw128(q + L::kQTile, 16, 1024);
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) mma_ss(t_s, dk_k + kstep_a(kk), dq_k + kstep_b(kk), id_s, kk > 0 ? 1u : 0u);
+            }
+            __syncwarp();
+            if (i >= 2) {
+                w = mbar_wait(bar(L::kDqFree + b), ((i - 2) >> 1) & 1, ctx);
+                if (!__all_sync(0xffffffffu, w)) return false;
+                tc_fence_after_sync();
+            }
+            if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(t_s + 64, dv_k + kstep_a(kk), ddo_k + kstep_b(kk), id_s, kk > 0 ? 1u : 0u);
+                mma_commit(bar(L::kSpFull + b));
+            }
+            __syncwarp();
+            return true;
+        };
+
         bool ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kKvFull), 0, ctx));
+        if (ok) ok = issue_sdp(0);
+        if (ok && n_iter > 1) ok = issue_sdp(1);
         for (int it = 0; it < n_iter && ok; ++it) {
-            const int s = it % kBwdStages;
-            const uint32_t ph = it & 1;
-            const uint32_t qbase = s_base + L::kRingOff + s * 2 * L::kTile;
-            const uint64_t dq_k = make_smem_desc_sw128(qbase, 16, 1024);                     // Q_i, K-major
-            const uint64_t ddo_k = make_smem_desc_sw128(qbase + L::kTile, 16, 1024);         // dO_i, K-major
-            const uint64_t dq_mn = make_smem_desc_sw128(qbase, 16384, 1024);                 // Q_i, MN-major
-            const uint64_t ddo_mn = make_smem_desc_sw128(qbase + L::kTile, 16384, 1024);     // dO_i, MN-major
-            bool w = mbar_wait(bar(L::kQFull + s), (it / kBwdStages) & 1, ctx);
-            w = w && mbar_wait(bar(L::kStFree), ph ^ 1u, ctx);  // previous dQ_i partial read out
-            if (!(ok = __all_sync(0xffffffffu, w))) break;
-            tc_fence_after_sync();
-            if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    mma_ss(t_st, dk_k + off, dq_k + off, id_nt, kk > 0 ? 1u : 0u);
-                }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    mma_ss(t_dp, dv_k + off, ddo_k + off, id_nt, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(bar(L::kSpFull));
-            }
-            __syncwarp();
+            const int b = it & 1;
+            const uint32_t ph = (it >> 1) & 1;
+            const uint32_t q = ring(it);
+            const uint32_t t_s = tmem + 2 * D + 128 * b;
+            const uint64_t dq_mn = make_smem_desc_sw128(q, L::kQBlock, 1024);               // Q_i, MN-major
+            const uint64_t ddo_mn = make_smem_desc_sw128(q + L::kQTile, L::kQBlock, 1024);  // dO_i, MN-major
+            const uint64_t dds_mn = make_smem_desc_sw128(s_base + L::kDsOff + b * L::kDsBuf, L::kDsBuf, 1024);
             // dV += P^T dO_i once P^T is in TMEM
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kPFull), ph, ctx)))) break;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kPFull + b), ph, ctx)))) break;
             tc_fence_after_sync();
             if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(t_dv, t_st + kk * 8, ddo_mn + static_cast<uint64_t>((kk * 2048) >> 4), id_tn,
-                           (it > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kBq / 16; ++kk)
+                    mma_ts(t_dv, t_s + kk * 8, ddo_mn + kk * kRows16, id_acc, (it > 0 || kk > 0) ? 1u : 0u);
             }
             __syncwarp();
-            // dK += dS^T Q_i and dQ_i = dS K_j once dS is ready
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kDsFull), ph, ctx)))) break;
+            // dK += dS^T Q_i and dQ_i^T = K_j^T dS^T once dS is ready
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kDsFull + b), ph, ctx)))) break;
             tc_fence_after_sync();
             if (elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(t_dk, t_dp + kk * 8, dq_mn + static_cast<uint64_t>((kk * 2048) >> 4), id_tn,
-                           (it > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kBq / 16; ++kk)
+                    mma_ts(t_dk, t_s + 64 + kk * 8, dq_mn + kk * kRows16, id_acc, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(t_st, dds_mn + static_cast<uint64_t>((kk * 2048) >> 4),
-                           dk_mn + static_cast<uint64_t>((kk * 2048) >> 4), id_mn, kk > 0 ? 1u : 0u);
-                mma_commit(bar(L::kDqFull));
-                mma_commit(bar(L::kDsEmpty));
-                mma_commit(bar(L::kQEmpty + s));
+                for (int kk = 0; kk < kBc / 16; ++kk)
+                    mma_ss(t_s + 64, dkt_mn + kk * kRows16, dds_mn + kk * kRows16, id_dq, kk > 0 ? 1u : 0u);
+                mma_commit(bar(L::kDqFull + b));
+                mma_commit(bar(L::kDsEmpty + b));
+                mma_commit(bar(L::kQEmpty + it % kBwdStages));
                 if (it == n_iter - 1) mma_commit(bar(L::kKvDone));
             }
             __syncwarp();
+            if (it + 2 < n_iter) ok = issue_sdp(it + 2);
         }
         if (elect_one()) mma_commit(bar(L::kDrain));
         __syncwarp();
         mbar_wait_drain(bar(L::kDrain), 0, 1000000000ull);
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ compute warpgroup
-        // Every tcgen05.ld/st below is warp-aligned: all 32 lanes execute it,
-        // whatever their row; only global stores and atomics are per-lane.
-        // The warps never wait on one another, only on mbarriers.
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ P and dS
+        // Thread r = key row r of the tile (TMEM lane r).  Every tcgen05.ld/st
+        // is executed by all 32 lanes of the warp; only stores are per-lane.
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;                 // key row in the tile (TMEM lane)
+        const int r = quad * 32 + lane;
         const int key = kt * kBc + r;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t t_st = tmem + lane_addr, t_dp = tmem + lane_addr + 128;
-        uint8_t* ds_s = smem + L::kDsOff;
         const float sl2 = p.scale_log2;
         const size_t head = static_cast<size_t>(bh) * p.N;
         const size_t stat_head = static_cast<size_t>(bh) * p.Np;
         bool ok = true;
         for (int it = 0; it < n_iter && ok; ++it) {
-            const int qt = i_first + it;
-            const uint32_t ph = it & 1;
-            const float* lse2 = p.lse2 + stat_head + static_cast<size_t>(qt) * kBr;   // this query tile's
-            const float* dvec = p.Dvec + stat_head + static_cast<size_t>(qt) * kBr;   // statistics
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kSpFull), ph, ctx));
+            const int b = it & 1;
+            const uint32_t ph = (it >> 1) & 1;
+            const int q0 = (i_first + it) * kBq;
+            const uint32_t t_s = tmem + lane_addr + 2 * D + 128 * b, t_dp = t_s + 64;
+            const float* lse2 = p.lse2 + stat_head + q0;
+            const float* dvec = p.Dvec + stat_head + q0;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kSpFull + b), ph, ctx));
             if (!ok) break;
             tc_fence_after_sync();
-            // P^T = exp2(S^T * scale * log2e - LSE * log2e), masked, -> bf16 over S^T's first 64 columns
-#pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            // P^T = exp2(S^T * scale * log2e - LSE * log2e), masked -> bf16 over S^T's first 32 columns
+#pragma unroll
+            for (int c0 = 0; c0 < kBq; c0 += 32) {
                 uint32_t sv[32];
-                tmem_ld32(t_st + c0, sv);
+                tmem_ld32(t_s + c0, sv);
                 float l[32];
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
@@ -262,30 +300,31 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
-                    const int q0 = qt * kBr + c0 + c;
+                    const int qa = q0 + c0 + c;
                     float a = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -l[c]));
-                    float b = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), sl2, -l[c + 1]));
-                    if (key >= p.N || (CAUSAL && key > q0)) a = 0.f;
-                    if (key >= p.N || (CAUSAL && key > q0 + 1)) b = 0.f;
-                    pk[c / 2] = pack_bf16x2(a, b);
+                    float bb = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), sl2, -l[c + 1]));
+                    if (key >= p.N || (CAUSAL && key > qa)) a = 0.f;
+                    if (key >= p.N || (CAUSAL && key > qa + 1)) bb = 0.f;
+                    pk[c / 2] = pack_bf16x2(a, bb);
                 }
-                tmem_st16(t_st + c0 / 2, pk);
+                tmem_st16(t_s + c0 / 2, pk);
             }
             tmem_wait_st();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kPFull));
+            if (lane == 0) mbar_arrive(bar(L::kPFull + b));
             __syncwarp();
-            // dS = scale * P * (dP - D): dS^T -> TMEM (dP^T's first 64 columns),
-            // dS -> shared memory (MN-major, 128-byte swizzled) for dQ_i = dS K_j.
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kDsEmpty), ph ^ 1u, ctx));
+            // dS = scale * P * (dP - D): dS^T -> TMEM over dP^T's first 32 columns,
+            // dS -> shared memory ([key][query], 128-byte swizzled) for dQ^T.
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kDsEmpty + b), ph ^ 1u, ctx));
             if (!ok) break;
             tc_fence_after_sync();
-#pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint8_t* ds_row = smem + L::kDsOff + b * L::kDsBuf + r * 128;
+#pragma unroll
+            for (int c0 = 0; c0 < kBq; c0 += 32) {
                 uint32_t dv[32], pv[16];
                 tmem_ld32(t_dp + c0, dv);
-                tmem_ld16(t_st + c0 / 2, pv);
+                tmem_ld16(t_s + c0 / 2, pv);
                 float dd[32];
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
@@ -299,16 +338,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 for (int c = 0; c < 32; c += 2) {
                     const float pa = __uint_as_float(pv[c / 2] << 16), pb = __uint_as_float(pv[c / 2] & 0xffff0000u);
                     const float a = p.scale * pa * (__uint_as_float(dv[c]) - dd[c]);
-                    const float b = p.scale * pb * (__uint_as_float(dv[c + 1]) - dd[c + 1]);
-                    pk[c / 2] = pack_bf16x2(a, b);
+                    const float bb = p.scale * pb * (__uint_as_float(dv[c + 1]) - dd[c + 1]);
+                    pk[c / 2] = pack_bf16x2(a, bb);
                 }
                 tmem_st16(t_dp + c0 / 2, pk);
-                // queries c0..c0+31 of key row r: four 16-byte chunks of block c0/64
-                uint8_t* rowp = ds_s + (c0 >> 6) * 16384 + r * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int ch = ((c0 & 63) >> 3) + q;
-                    *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
+                    const int ch = (c0 >> 3) + q;  // 16-byte chunk of the 128-byte row
+                    *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) << 4)) =
                         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
             }
@@ -316,58 +353,99 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             tmem_wait_st();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kDsFull));
-            __syncwarp();
-            // dQ_i partial (TMEM lane = query row) -> fp32 atomics into the accumulator
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kDqFull), ph, ctx));
-            if (!ok) break;
-            tc_fence_after_sync();
-            const int qrow = qt * kBr + r;
-            const bool row_ok = qrow < p.N;
-            float* dqrow = p.dQacc + (head + (row_ok ? qrow : 0)) * D;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(t_st + c0, v);
-                tmem_wait_ld(v);
-                if (row_ok) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        atomicAdd(reinterpret_cast<float4*>(dqrow + c0 + c),
-                                  make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]),
-                                              __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])));
-                }
-                __syncwarp();
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kStFree));
+            if (lane == 0) mbar_arrive(bar(L::kDsFull + b));
             __syncwarp();
         }
-        // dK, dV of this key tile -> bf16 (all lanes read TMEM; rows past N store nothing)
+        // dV of this key tile -> bf16 (all lanes read TMEM; rows past N store nothing)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kKvDone), 0, ctx));
         if (ok) {
             tc_fence_after_sync();
             const bool key_ok = key < p.N;
+            uint4* dst = reinterpret_cast<uint4*>(p.dV + (head + (key_ok ? key : 0)) * D);
 #pragma unroll 1
-            for (int g = 0; g < 2; ++g) {
-                const uint32_t src = tmem + lane_addr + 256 + (g == 0 ? D : 0);  // dK, then dV
-                uint4* dst = reinterpret_cast<uint4*>((g == 0 ? p.dK : p.dV) + (head + (key_ok ? key : 0)) * D);
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(src + c0, v);
-                    tmem_wait_ld(v);
-                    uint32_t wv[16];
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_addr + c0, v);
+                tmem_wait_ld(v);
+                uint32_t wv[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) wv[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                    if (key_ok) {
+                for (int i = 0; i < 16; ++i) wv[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                if (key_ok) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[c0 / 8 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
-                    }
-                    __syncwarp();
+                    for (int i = 0; i < 4; ++i)
+                        dst[c0 / 8 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
                 }
+                __syncwarp();
+            }
+        }
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ dQ readout
+        // Thread r = head-dim column r of dQ_i^T (TMEM lane r).  For each query c
+        // of the block the 32 lanes of a warp add 32 consecutive floats of row
+        // q0 + c of the accumulator: one 128-byte line per instruction.
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        const size_t head = static_cast<size_t>(bh) * p.N;
+        const bool col_ok = r < D;  // warp-uniform: d is a multiple of 32
+        bool ok = true;
+        for (int it = 0; it < n_iter && ok; ++it) {
+            const int b = it & 1;
+            const uint32_t ph = (it >> 1) & 1;
+            const int q0 = (i_first + it) * kBq;
+            const uint32_t t_dq = tmem + lane_addr + 2 * D + 128 * b + 64;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kDqFull + b), ph, ctx));
+            if (!ok) break;
+            tc_fence_after_sync();
+            uint32_t v0[32], v1[32];
+            tmem_ld32(t_dq, v0);
+            tmem_ld32(t_dq + 32, v1);
+            tmem_wait_ld(v0);
+            tmem_wait_ld(v1);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kDqFree + b));
+            __syncwarp();
+            if (col_ok) {
+                float* col = p.dQacc + (head + q0) * D + r;
+                const int nq = min(kBq, p.N - q0);  // warp-uniform
+                if (nq == kBq) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) atomicAdd(col + c * D, __uint_as_float(v0[c]));
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) atomicAdd(col + (32 + c) * D, __uint_as_float(v1[c]));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (c < nq) atomicAdd(col + c * D, __uint_as_float(v0[c]));
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (32 + c < nq) atomicAdd(col + (32 + c) * D, __uint_as_float(v1[c]));
+                }
+            }
+            __syncwarp();
+        }
+        // dK of this key tile -> bf16
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kKvDone), 0, ctx));
+        if (ok) {
+            tc_fence_after_sync();
+            const int key = kt * kBc + r;
+            const bool key_ok = key < p.N;
+            uint4* dst = reinterpret_cast<uint4*>(p.dK + (head + (key_ok ? key : 0)) * D);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_addr + D + c0, v);
+                tmem_wait_ld(v);
+                uint32_t wv[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) wv[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                if (key_ok) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[c0 / 8 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                }
+                __syncwarp();
             }
         }
     }
@@ -380,7 +458,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     }
 }
 
-// Per-row statistics of the backward, on rows padded to whole query tiles
+// Per-row statistics of the backward, on rows padded to whole key tiles
 // (Np = ceil(N / 128) * 128 per (batch, head)):
 //     D_i = sum_c dO_ic O_ic (fp32), lse2_i = LSE_i * log2(e);
 // padding rows get D = 0 and lse2 = +inf (so that exp2(. - lse2) = 0 there).
