@@ -37,7 +37,7 @@ METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak at N=
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "sm103_ptx.cuh", "plan.h", "attn_api.cu", "api_common.h"]
+KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "sm103_ptx.cuh", "plan.h", "plan.cpp", "attn_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 

@@ -23,8 +23,14 @@ struct DeviceState {
     bool bwd_smem_configured[2][2] = {{false, false}, {false, false}};  // backward <d == 128><causal>
 };
 
+// The cudaError_t of this thread's most recent ATTN_ERR_CUDA.
+extern thread_local int g_last_cuda_error;
+
 // Records `e` as this thread's last CUDA error and returns ATTN_ERR_CUDA.
 int cuda_fail(cudaError_t e);
+
+// Looks up the driver's cuTensorMapEncodeTiled once per process.
+int resolve_tensor_map_encoder();
 
 // The current device's state, set up on first use (checks for sm_103,
 // resolves the tensor-map encoder, allocates the error word).
@@ -34,6 +40,10 @@ int device_state(DeviceState** out);
 // 64 columns x box_rows rows with the 128-byte swizzle the tcgen05
 // descriptors expect.  Rows past N read as zero.
 int encode_rows_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
+
+// An fp32 tensor viewed as [BH][N][d], written by TMA (reduce-add) in boxes of
+// d columns x box_rows rows, unswizzled.  Rows past N are dropped.
+int encode_f32_rows_map(CUtensorMap* map, void* base, int BH, int N, int d, int box_rows);
 
 bool aligned16(const void* p);
 

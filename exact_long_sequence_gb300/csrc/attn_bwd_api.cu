@@ -16,7 +16,7 @@ namespace {
 
 template <int D, bool CAUSAL>
 int launch_bwd(DeviceState& dev, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tdo, const BwdParams& p, int BH, cudaStream_t stream) {
+               const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p, int BH, cudaStream_t stream) {
     auto kernel = attn_bwd_kernel<D, CAUSAL>;
     bool& configured = dev.bwd_smem_configured[D == 128][CAUSAL];
     cudaError_t e;
@@ -26,7 +26,7 @@ int launch_bwd(DeviceState& dev, const CUtensorMap& tq, const CUtensorMap& tk, c
             return cuda_fail(e);
         configured = true;
     }
-    kernel<<<BH * p.num_k_tiles, kBwdThreads, BwdLayout<D>::kSmem, stream>>>(tq, tk, tv, tdo, p);
+    kernel<<<BH * p.num_k_tiles, kBwdThreads, BwdLayout<D>::kSmem, stream>>>(tq, tk, tv, tdo, tdq, p);
     e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -65,11 +65,12 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
     float* dqacc = static_cast<float*>(workspace);
     float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * d * 4));
     float* lse2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dvec) + align256(padded * 4));
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if ((st = encode_rows_map(&tq, Q, BH, N, d, kBq)) != ATTN_OK ||
         (st = encode_rows_map(&tk, K, BH, N, d, kBc)) != ATTN_OK ||
         (st = encode_rows_map(&tv, V, BH, N, d, kBc)) != ATTN_OK ||
-        (st = encode_rows_map(&tdo, dO, BH, N, d, kBq)) != ATTN_OK)
+        (st = encode_rows_map(&tdo, dO, BH, N, d, kBq)) != ATTN_OK ||
+        (st = encode_f32_rows_map(&tdq, dqacc, BH, N, d, kBq)) != ATTN_OK)
         return st;
 
     // D_i = sum_c dO_ic O_ic and LSE_i * log2(e) on tile-padded rows; the dQ accumulator zeroed
@@ -100,11 +101,11 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
     p.scale_log2 = scale * 1.4426950408889634f;
     p.scale = scale;
     if (d == 64)
-        st = causal ? launch_bwd<64, true>(*dev, tq, tk, tv, tdo, p, BH, stream)
-                    : launch_bwd<64, false>(*dev, tq, tk, tv, tdo, p, BH, stream);
+        st = causal ? launch_bwd<64, true>(*dev, tq, tk, tv, tdo, tdq, p, BH, stream)
+                    : launch_bwd<64, false>(*dev, tq, tk, tv, tdo, tdq, p, BH, stream);
     else
-        st = causal ? launch_bwd<128, true>(*dev, tq, tk, tv, tdo, p, BH, stream)
-                    : launch_bwd<128, false>(*dev, tq, tk, tv, tdo, p, BH, stream);
+        st = causal ? launch_bwd<128, true>(*dev, tq, tk, tv, tdo, tdq, p, BH, stream)
+                    : launch_bwd<128, false>(*dev, tq, tk, tv, tdo, tdq, p, BH, stream);
     if (st != ATTN_OK) return st;
     // dQ = bf16(accumulator)
     const size_t n4 = rows * d / 4;

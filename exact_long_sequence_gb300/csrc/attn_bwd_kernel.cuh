@@ -19,9 +19,11 @@
 //     dQ_i^T = K_j^T dS^T  M = d (padded to 128), N = 64  (A = K_j read transposed)
 // S^T and dP^T are double-buffered in TMEM, so the tensor core computes the
 // scores of block i+2 while the compute warps still work on block i.  dQ is
-// produced transposed so that TMEM lane = head-dim column: the readout warps
-// then add it to the fp32 accumulator with one full 128-byte line per warp
-// instruction, and they release the TMEM columns before issuing the adds.
+// produced transposed (TMEM lane = head-dim column); the readout warps copy it
+// to registers, release the TMEM columns, stage it in shared memory as
+// [query][d] fp32 and add it to the fp32 accumulator in global memory with one
+// TMA bulk reduce per block.  The per-query LSE and D of a block arrive by TMA
+// with its Q_i and dO_i.
 //
 // Warp roles: 0 TMA producer, 1 MMA issuer, 4-7 P and dS (thread = key row),
 // 8-11 dQ readout (thread = head-dim column); at the end 4-7 write dV and
@@ -36,13 +38,16 @@
 #include <cstdint>
 
 #include "plan.h"
+#include "sm103_bulk.cuh"
 #include "sm103_ptx.cuh"
 
 namespace elsattn {
 
 constexpr int kBwdThreads = 384;  // warps 0 TMA, 1 MMA, 4-7 P/dS, 8-11 dQ readout
 constexpr int kBq = 64;           // queries per block
-constexpr int kBwdStages = 4;     // Q_i + dO_i ring depth
+// Q_i + dO_i ring depth: three blocks are in flight (i, i+1 and the i+2 whose
+// scores are computed ahead), so three stages suffice.
+constexpr int bwd_stages(int d) { return d == 128 ? 3 : 4; }
 
 struct BwdParams {
     float* dQacc;          // [BH, N, d] fp32, zeroed; receives scale * dS K
@@ -62,6 +67,7 @@ struct BwdParams {
 
 template <int D>
 struct BwdLayout {
+    static constexpr int kBwdStages = bwd_stages(D);
     static constexpr int kKvTile = 128 * D * 2;             // K_j or V_j: [128 keys x d] bf16
     static constexpr int kQTile = kBq * D * 2;              // Q_i or dO_i: [64 queries x d] bf16
     static constexpr int kKvBlock = 128 * 128;              // one 64-column block of a K/V tile
@@ -72,7 +78,10 @@ struct BwdLayout {
     static constexpr int kStageBytes = 2 * kQTile;
     static constexpr int kDsOff = kRingOff + kBwdStages * kStageBytes;  // [2][128 keys][64 queries] bf16
     static constexpr int kDsBuf = 128 * kBq * 2;
-    static constexpr int kBarOff = kDsOff + 2 * kDsBuf;
+    static constexpr int kDqOff = kDsOff + 2 * kDsBuf;     // [64 queries][d] fp32: dQ_i staged for the reduce
+    static constexpr int kStatOff = kDqOff + kBq * D * 4;  // [stage][lse2 x 64, D x 64] fp32
+    static constexpr int kStatBytes = 2 * kBq * 4;
+    static constexpr int kBarOff = kStatOff + kBwdStages * kStatBytes;
     // barriers
     static constexpr int kKvFull = 0;
     static constexpr int kQFull = 1;                         // [kBwdStages]
@@ -83,7 +92,9 @@ struct BwdLayout {
     static constexpr int kDsEmpty = kDsFull + 2;             // [2] dQ^T MMA done reading dS
     static constexpr int kDqFull = kDsEmpty + 2;             // [2] dQ^T of a block complete
     static constexpr int kDqFree = kDqFull + 2;              // [2] dQ^T read out of TMEM (4)
-    static constexpr int kKvDone = kDqFree + 2;              // dK, dV accumulation complete
+    static constexpr int kStFull = kDqFree + 2;              // dQ_i written to the staging buffer (4)
+    static constexpr int kStEmpty = kStFull + 1;             // the reduce has read the staging buffer
+    static constexpr int kKvDone = kStEmpty + 1;             // dK, dV accumulation complete
     static constexpr int kDrain = kKvDone + 1;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr int kFlagsOff = kBarOff + kNumBars * 8;
@@ -99,8 +110,9 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
     using L = BwdLayout<D>;
+    constexpr int kBwdStages = L::kBwdStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
@@ -132,6 +144,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             mbar_init(bar(L::kDqFull + b), 1);
             mbar_init(bar(L::kDqFree + b), 4);
         }
+        mbar_init(bar(L::kStFull), 4);
+        mbar_init(bar(L::kStEmpty), 1);
         mbar_init(bar(L::kKvDone), 1);
         mbar_init(bar(L::kDrain), 1);
         fence_barrier_init();
@@ -159,9 +173,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const int s = it % kBwdStages;
             ok = mbar_wait(bar(L::kQEmpty + s), ((it / kBwdStages) & 1) ^ 1, ctx);
             if (!ok) break;
-            mbar_arrive_expect_tx(bar(L::kQFull + s), L::kStageBytes);
+            mbar_arrive_expect_tx(bar(L::kQFull + s), L::kStageBytes + L::kStatBytes);
             const uint32_t dst = s_base + L::kRingOff + s * L::kStageBytes;
             const int row = (i_first + it) * kBq;
+            const size_t stat = static_cast<size_t>(bh) * p.Np + row;
+            const uint32_t sdst = s_base + L::kStatOff + s * L::kStatBytes;
+            bulk_load(sdst, p.lse2 + stat, kBq * 4, bar(L::kQFull + s));
+            bulk_load(sdst + kBq * 4, p.Dvec + stat, kBq * 4, bar(L::kQFull + s));
 #pragma unroll
             for (int b = 0; b < D / 64; ++b) {
                 tma_load_3d(dst + b * L::kQBlock, &tmap_q, bar(L::kQFull + s), b * 64, row, bh);
@@ -273,16 +291,18 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         const float sl2 = p.scale_log2;
         const size_t head = static_cast<size_t>(bh) * p.N;
-        const size_t stat_head = static_cast<size_t>(bh) * p.Np;
         bool ok = true;
         for (int it = 0; it < n_iter && ok; ++it) {
             const int b = it & 1;
             const uint32_t ph = (it >> 1) & 1;
             const int q0 = (i_first + it) * kBq;
             const uint32_t t_s = tmem + lane_addr + 2 * D + 128 * b, t_dp = t_s + 64;
-            const float* lse2 = p.lse2 + stat_head + q0;
-            const float* dvec = p.Dvec + stat_head + q0;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kSpFull + b), ph, ctx));
+            const int s = it % kBwdStages;
+            const float* lse2 = reinterpret_cast<const float*>(smem + L::kStatOff + s * L::kStatBytes);
+            const float* dvec = lse2 + kBq;
+            // S^T of the block, and the block's statistics (they land with Q_i)
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kSpFull + b), ph, ctx) &&
+                                             mbar_wait(bar(L::kQFull + s), (it / kBwdStages) & 1, ctx));
             if (!ok) break;
             tc_fence_after_sync();
             // P^T = exp2(S^T * scale * log2e - LSE * log2e), masked -> bf16 over S^T's first 32 columns
@@ -293,7 +313,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 float l[32];
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
-                    const float4 t = __ldg(reinterpret_cast<const float4*>(lse2 + c0 + c));
+                    const float4 t = *reinterpret_cast<const float4*>(lse2 + c0 + c);
                     l[c] = t.x, l[c + 1] = t.y, l[c + 2] = t.z, l[c + 3] = t.w;
                 }
                 tmem_wait_ld(sv);
@@ -328,7 +348,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 float dd[32];
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
-                    const float4 t = __ldg(reinterpret_cast<const float4*>(dvec + c0 + c));
+                    const float4 t = *reinterpret_cast<const float4*>(dvec + c0 + c);
                     dd[c] = t.x, dd[c + 1] = t.y, dd[c + 2] = t.z, dd[c + 3] = t.w;
                 }
                 tmem_wait_ld(dv);
@@ -380,14 +400,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dQ readout
-        // Thread r = head-dim column r of dQ_i^T (TMEM lane r).  For each query c
-        // of the block the 32 lanes of a warp add 32 consecutive floats of row
-        // q0 + c of the accumulator: one 128-byte line per instruction.
+        // Thread r = head-dim column r of dQ_i^T (TMEM lane r).  The block's dQ_i is
+        // staged in shared memory as [64 queries][d] fp32 (a warp writes 32
+        // consecutive floats of a row per store) and added to the accumulator
+        // by one TMA reduce; rows past N fall outside the tensor and are dropped.
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         const size_t head = static_cast<size_t>(bh) * p.N;
         const bool col_ok = r < D;  // warp-uniform: d is a multiple of 32
+        const bool issuer = warp == 8 && lane == 0;
+        float* stage = reinterpret_cast<float*>(smem + L::kDqOff);
         bool ok = true;
         for (int it = 0; it < n_iter && ok; ++it) {
             const int b = it & 1;
@@ -406,25 +429,31 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kDqFree + b));
             __syncwarp();
+            // the staging buffer is free once the previous block's reduce has read it
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kStEmpty), (it & 1) ^ 1u, ctx));
+            if (!ok) break;
             if (col_ok) {
-                float* col = p.dQacc + (head + q0) * D + r;
-                const int nq = min(kBq, p.N - q0);  // warp-uniform
-                if (nq == kBq) {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) atomicAdd(col + c * D, __uint_as_float(v0[c]));
+                for (int c = 0; c < 32; ++c) stage[c * D + r] = __uint_as_float(v0[c]);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) atomicAdd(col + (32 + c) * D, __uint_as_float(v1[c]));
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (c < nq) atomicAdd(col + c * D, __uint_as_float(v0[c]));
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (32 + c < nq) atomicAdd(col + (32 + c) * D, __uint_as_float(v1[c]));
-                }
+                for (int c = 0; c < 32; ++c) stage[(32 + c) * D + r] = __uint_as_float(v1[c]);
             }
+            fence_proxy_async_smem();  // staged by threads, read by the TMA unit
             __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kStFull));
+            bool w = true;
+            if (issuer) {
+                w = mbar_wait(bar(L::kStFull), it & 1, ctx);
+                if (w) {
+                    tma_reduce_add_3d(&tmap_dq, s_base + L::kDqOff, 0, q0, bh);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();
+                }
+                mbar_arrive(bar(L::kStEmpty));
+            }
+            ok = __all_sync(0xffffffffu, w);
         }
+        if (issuer) bulk_wait_group0();  // every reduce has landed before the CTA ends
         // dK of this key tile -> bf16
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kKvDone), 0, ctx));
         if (ok) {
