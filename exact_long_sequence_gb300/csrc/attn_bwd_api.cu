@@ -70,7 +70,7 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
         (st = encode_rows_map(&tk, K, BH, N, d, kBc)) != ATTN_OK ||
         (st = encode_rows_map(&tv, V, BH, N, d, kBc)) != ATTN_OK ||
         (st = encode_rows_map(&tdo, dO, BH, N, d, kBq)) != ATTN_OK ||
-        (st = encode_f32_rows_map(&tdq, dqacc, BH, N, d, kBq)) != ATTN_OK)
+        (st = encode_f32_rows_map(&tdq, dqacc, BH, N, d, kBq / 2)) != ATTN_OK)
         return st;
 
     // D_i = sum_c dO_ic O_ic and LSE_i * log2(e) on tile-padded rows; the dQ accumulator zeroed

@@ -78,7 +78,7 @@ struct BwdLayout {
     static constexpr int kStageBytes = 2 * kQTile;
     static constexpr int kDsOff = kRingOff + kBwdStages * kStageBytes;  // [2][128 keys][64 queries] bf16
     static constexpr int kDsBuf = 128 * kBq * 2;
-    static constexpr int kDqOff = kDsOff + 2 * kDsBuf;     // [64 queries][d] fp32: dQ_i staged for the reduce
+    static constexpr int kDqOff = kDsOff + 2 * kDsBuf;     // [2 halves][32 queries][d] fp32: dQ_i staged
     static constexpr int kStatOff = kDqOff + kBq * D * 4;  // [stage][lse2 x 64, D x 64] fp32
     static constexpr int kStatBytes = 2 * kBq * 4;
     static constexpr int kBarOff = kStatOff + kBwdStages * kStatBytes;
@@ -92,9 +92,9 @@ struct BwdLayout {
     static constexpr int kDsEmpty = kDsFull + 2;             // [2] dQ^T MMA done reading dS
     static constexpr int kDqFull = kDsEmpty + 2;             // [2] dQ^T of a block complete
     static constexpr int kDqFree = kDqFull + 2;              // [2] dQ^T read out of TMEM (4)
-    static constexpr int kStFull = kDqFree + 2;              // dQ_i written to the staging buffer (4)
-    static constexpr int kStEmpty = kStFull + 1;             // the reduce has read the staging buffer
-    static constexpr int kKvDone = kStEmpty + 1;             // dK, dV accumulation complete
+    static constexpr int kStFull = kDqFree + 2;              // [2] a half of dQ_i staged (4)
+    static constexpr int kStEmpty = kStFull + 2;             // [2] the reduce has read that half
+    static constexpr int kKvDone = kStEmpty + 2;             // dK, dV accumulation complete
     static constexpr int kDrain = kKvDone + 1;
     static constexpr int kNumBars = kDrain + 1;
     static constexpr int kFlagsOff = kBarOff + kNumBars * 8;
@@ -144,8 +144,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             mbar_init(bar(L::kDqFull + b), 1);
             mbar_init(bar(L::kDqFree + b), 4);
         }
-        mbar_init(bar(L::kStFull), 4);
-        mbar_init(bar(L::kStEmpty), 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(L::kStFull + h), 4);
+            mbar_init(bar(L::kStEmpty + h), 1);
+        }
         mbar_init(bar(L::kKvDone), 1);
         mbar_init(bar(L::kDrain), 1);
         fence_barrier_init();
@@ -401,16 +403,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     } else if (warp >= 8) {
         // ------------------------------------------------------------ dQ readout
         // Thread r = head-dim column r of dQ_i^T (TMEM lane r).  The block's dQ_i is
-        // staged in shared memory as [64 queries][d] fp32 (a warp writes 32
-        // consecutive floats of a row per store) and added to the accumulator
-        // by one TMA reduce; rows past N fall outside the tensor and are dropped.
+        // staged in shared memory as two halves of [32 queries][d] fp32 (a warp
+        // writes 32 consecutive floats of a row per store), and each half is added
+        // to the accumulator by one TMA reduce while the other half is staged.
+        // Rows past N fall outside the tensor and are dropped.  One thread issues
+        // the reduces; it releases a half once the reduce issued before the
+        // current one has read its data.
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         const size_t head = static_cast<size_t>(bh) * p.N;
         const bool col_ok = r < D;  // warp-uniform: d is a multiple of 32
         const bool issuer = warp == 8 && lane == 0;
-        float* stage = reinterpret_cast<float*>(smem + L::kDqOff);
+        constexpr int kHalf = kBq / 2;
         bool ok = true;
         for (int it = 0; it < n_iter && ok; ++it) {
             const int b = it & 1;
@@ -420,40 +425,43 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kDqFull + b), ph, ctx));
             if (!ok) break;
             tc_fence_after_sync();
-            uint32_t v0[32], v1[32];
-            tmem_ld32(t_dq, v0);
-            tmem_ld32(t_dq + 32, v1);
-            tmem_wait_ld(v0);
-            tmem_wait_ld(v1);
+            uint32_t v[2][32];
+            tmem_ld32(t_dq, v[0]);
+            tmem_ld32(t_dq + 32, v[1]);
+            tmem_wait_ld(v[0]);
+            tmem_wait_ld(v[1]);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::kDqFree + b));
             __syncwarp();
-            // the staging buffer is free once the previous block's reduce has read it
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kStEmpty), (it & 1) ^ 1u, ctx));
-            if (!ok) break;
-            if (col_ok) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) stage[c * D + r] = __uint_as_float(v0[c]);
+            for (int h = 0; h < 2 && ok; ++h) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kStEmpty + h), (it & 1) ^ 1u, ctx));
+                if (!ok) break;
+                float* stage = reinterpret_cast<float*>(smem + L::kDqOff + h * kHalf * D * 4);
+                if (col_ok) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) stage[(32 + c) * D + r] = __uint_as_float(v1[c]);
-            }
-            fence_proxy_async_smem();  // staged by threads, read by the TMA unit
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kStFull));
-            bool w = true;
-            if (issuer) {
-                w = mbar_wait(bar(L::kStFull), it & 1, ctx);
-                if (w) {
-                    tma_reduce_add_3d(&tmap_dq, s_base + L::kDqOff, 0, q0, bh);
-                    bulk_commit_group();
-                    bulk_wait_group_read0();
+                    for (int c = 0; c < kHalf; ++c) stage[c * D + r] = __uint_as_float(v[h][c]);
                 }
-                mbar_arrive(bar(L::kStEmpty));
+                fence_proxy_async_smem();  // staged by threads, read by the TMA unit
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kStFull + h));
+                bool w = true;
+                if (issuer) {
+                    w = mbar_wait(bar(L::kStFull + h), it & 1, ctx);
+                    if (w) {
+                        tma_reduce_add_3d(&tmap_dq, s_base + L::kDqOff + h * kHalf * D * 4, 0, q0 + h * kHalf, bh);
+                        bulk_commit_group();
+                    }
+                    // the reduce issued before this one has read its half: release it
+                    bulk_wait_group_read<1>();
+                    if (h == 1) mbar_arrive(bar(L::kStEmpty + 0));
+                    else if (it > 0) mbar_arrive(bar(L::kStEmpty + 1));
+                }
+                ok = __all_sync(0xffffffffu, w);
             }
-            ok = __all_sync(0xffffffffu, w);
         }
-        if (issuer) bulk_wait_group0();  // every reduce has landed before the CTA ends
+        if (issuer) bulk_wait_group<0>();  // every reduce has landed before the CTA ends
         // dK of this key tile -> bf16
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kKvDone), 0, ctx));
         if (ok) {

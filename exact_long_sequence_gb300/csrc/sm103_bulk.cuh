@@ -30,12 +30,16 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// Wait until no committed bulk group of this thread still reads shared memory.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// Wait until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
-// Wait until every committed bulk group of this thread has completed.
-__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until at most N committed bulk groups of this thread are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
 
 }  // namespace elsattn
