@@ -25,13 +25,14 @@
 // TMA bulk reduce per block.  The per-query LSE and D of a block arrive by TMA
 // with its Q_i and dO_i.
 //
-// Warp roles: 0 TMA producer, 1 MMA issuer, 4-7 P and dS (thread = key row),
-// 8-11 dQ readout (thread = head-dim column); at the end 4-7 write dV and
-// 8-11 write dK.
+// Warp roles: 0 TMA producer, 1 MMA issuer, 4-7 and 12-15 P and dS (thread =
+// key row; each warpgroup takes half of the block's queries), 8-11 dQ readout
+// (thread = head-dim column); at the end 4-7 and 12-15 write dV, 8-11 dK.
 //
 // TMEM columns: [0, d) dV | [d, 2d) dK | buffer b at 2d + 128 b:
-//   [0, 64) S^T, P^T (bf16) over its first 32;  [64, 128) dP^T, dS^T (bf16)
-//   over its first 32, then dQ^T of the block (fp32).
+//   [0, 64) S^T, then P^T (bf16) of queries 0-31 over [0, 16) and of queries
+//   32-63 over [32, 48);  [64, 128) dP^T, then dS^T likewise, then dQ^T of the
+//   block (fp32).
 #pragma once
 
 #include <cuda.h>
@@ -43,7 +44,7 @@
 
 namespace elsattn {
 
-constexpr int kBwdThreads = 384;  // warps 0 TMA, 1 MMA, 4-7 P/dS, 8-11 dQ readout
+constexpr int kBwdThreads = 512;  // warps 0 TMA, 1 MMA, 4-7 and 12-15 P/dS, 8-11 dQ readout
 constexpr int kBq = 64;           // queries per block
 // Q_i + dO_i ring depth: three blocks are in flight (i, i+1 and the i+2 whose
 // scores are computed ahead), so three stages suffice.
@@ -87,8 +88,8 @@ struct BwdLayout {
     static constexpr int kQFull = 1;                         // [kBwdStages]
     static constexpr int kQEmpty = kQFull + kBwdStages;      // [kBwdStages]
     static constexpr int kSpFull = kQEmpty + kBwdStages;     // [2] S^T and dP^T of a block complete
-    static constexpr int kPFull = kSpFull + 2;               // [2] P^T in TMEM (4 warp arrivals)
-    static constexpr int kDsFull = kPFull + 2;               // [2] dS^T in TMEM, dS in shared memory (4)
+    static constexpr int kPFull = kSpFull + 2;               // [2] P^T in TMEM (8 warp arrivals)
+    static constexpr int kDsFull = kPFull + 2;               // [2] dS^T in TMEM, dS in shared memory (8)
     static constexpr int kDsEmpty = kDsFull + 2;             // [2] dQ^T MMA done reading dS
     static constexpr int kDqFull = kDsEmpty + 2;             // [2] dQ^T of a block complete
     static constexpr int kDqFree = kDqFull + 2;              // [2] dQ^T read out of TMEM (4)
@@ -138,8 +139,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::kSpFull + b), 1);
-            mbar_init(bar(L::kPFull + b), 4);
-            mbar_init(bar(L::kDsFull + b), 4);
+            mbar_init(bar(L::kPFull + b), 8);
+            mbar_init(bar(L::kDsFull + b), 8);
             mbar_init(bar(L::kDsEmpty + b), 1);
             mbar_init(bar(L::kDqFull + b), 1);
             mbar_init(bar(L::kDqFree + b), 4);
@@ -208,6 +209,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         auto kstep_a = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * L::kKvBlock + (kk & 3) * 32) >> 4); };
         auto kstep_b = [](int kk) { return static_cast<uint64_t>(((kk >> 2) * L::kQBlock + (kk & 3) * 32) >> 4); };
         constexpr uint64_t kRows16 = (16 * 128) >> 4;  // 16 rows of an MN-major operand
+        // TMEM column of the bf16 A operand (P^T or dS^T) for queries 16 kk .. 16 kk + 15:
+        // each compute warpgroup packs its 32 queries over the first 16 of its own 32 columns.
+        auto a_col = [](int kk) { return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8); };
 
         // S^T and dP^T of block i into buffer i & 1.  The S^T half is free: P^T of
         // block i - 2 was read by dV (issued earlier) and by the dS pass (its
@@ -259,7 +263,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kBq / 16; ++kk)
-                    mma_ts(t_dv, t_s + kk * 8, ddo_mn + kk * kRows16, id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(t_dv, t_s + a_col(kk), ddo_mn + kk * kRows16, id_acc, (it > 0 || kk > 0) ? 1u : 0u);
             }
             __syncwarp();
             // dK += dS^T Q_i and dQ_i^T = K_j^T dS^T once dS is ready
@@ -268,7 +272,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kBq / 16; ++kk)
-                    mma_ts(t_dk, t_s + 64 + kk * 8, dq_mn + kk * kRows16, id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(t_dk, t_s + 64 + a_col(kk), dq_mn + kk * kRows16, id_acc, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < kBc / 16; ++kk)
                     mma_ss(t_s + 64, dkt_mn + kk * kRows16, dds_mn + kk * kRows16, id_dq, kk > 0 ? 1u : 0u);
@@ -283,11 +287,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         if (elect_one()) mma_commit(bar(L::kDrain));
         __syncwarp();
         mbar_wait_drain(bar(L::kDrain), 0, 1000000000ull);
-    } else if (warp >= 4 && warp < 8) {
+    } else if ((warp >= 4 && warp < 8) || warp >= 12) {
         // ------------------------------------------------------------ P and dS
-        // Thread r = key row r of the tile (TMEM lane r).  Every tcgen05.ld/st
+        // Thread r = key row r of the tile (TMEM lane r).  Warps 4-7 take the
+        // block's queries 0-31, warps 12-15 queries 32-63.  Every tcgen05.ld/st
         // is executed by all 32 lanes of the warp; only stores are per-lane.
         const int quad = warp & 3;
+        const int c0 = warp >= 12 ? 32 : 0;  // this warpgroup's query columns
         const int r = quad * 32 + lane;
         const int key = kt * kBc + r;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
@@ -308,8 +314,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (!ok) break;
             tc_fence_after_sync();
             // P^T = exp2(S^T * scale * log2e - LSE * log2e), masked -> bf16 over S^T's first 32 columns
-#pragma unroll
-            for (int c0 = 0; c0 < kBq; c0 += 32) {
+            {
                 uint32_t sv[32];
                 tmem_ld32(t_s + c0, sv);
                 float l[32];
@@ -329,7 +334,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     if (key >= p.N || (CAUSAL && key > qa + 1)) bb = 0.f;
                     pk[c / 2] = pack_bf16x2(a, bb);
                 }
-                tmem_st16(t_s + c0 / 2, pk);
+                tmem_st16(t_s + c0, pk);  // over this warpgroup's own S^T columns
             }
             tmem_wait_st();
             tc_fence_before_sync();
@@ -342,11 +347,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (!ok) break;
             tc_fence_after_sync();
             uint8_t* ds_row = smem + L::kDsOff + b * L::kDsBuf + r * 128;
-#pragma unroll
-            for (int c0 = 0; c0 < kBq; c0 += 32) {
+            {
                 uint32_t dv[32], pv[16];
                 tmem_ld32(t_dp + c0, dv);
-                tmem_ld16(t_s + c0 / 2, pv);
+                tmem_ld16(t_s + c0, pv);
                 float dd[32];
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
@@ -363,7 +367,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     const float bb = p.scale * pb * (__uint_as_float(dv[c + 1]) - dd[c + 1]);
                     pk[c / 2] = pack_bf16x2(a, bb);
                 }
-                tmem_st16(t_dp + c0 / 2, pk);
+                tmem_st16(t_dp + c0, pk);  // over this warpgroup's own dP^T columns
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int ch = (c0 >> 3) + q;  // 16-byte chunk of the 128-byte row
@@ -378,16 +382,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (lane == 0) mbar_arrive(bar(L::kDsFull + b));
             __syncwarp();
         }
-        // dV of this key tile -> bf16 (all lanes read TMEM; rows past N store nothing)
+        // dV of this key tile -> bf16, half of its columns per warpgroup (all lanes
+        // read TMEM; rows past N store nothing)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kKvDone), 0, ctx));
         if (ok) {
             tc_fence_after_sync();
             const bool key_ok = key < p.N;
             uint4* dst = reinterpret_cast<uint4*>(p.dV + (head + (key_ok ? key : 0)) * D);
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int cv = (c0 ? D / 2 : 0); cv < (c0 ? D : D / 2); cv += 32) {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_addr + c0, v);
+                tmem_ld32(tmem + lane_addr + cv, v);
                 tmem_wait_ld(v);
                 uint32_t wv[16];
 #pragma unroll
@@ -395,12 +400,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (key_ok) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        dst[c0 / 8 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+                        dst[cv / 8 + i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
                 }
                 __syncwarp();
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 8 && warp < 12) {
         // ------------------------------------------------------------ dQ readout
         // Thread r = head-dim column r of dQ_i^T (TMEM lane r).  The block's dQ_i is
         // staged in shared memory as two halves of [32 queries][d] fp32 (a warp
