@@ -13,6 +13,11 @@ the events. `e2e` times the same pass through the host-buffer C-ABI entry
 `--impl reference` times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of query rows of the same workload.
 
+`--pass bwd` times the backward instead (attn_bwd: dQ, dK, dV from Q, K, V, O,
+LSE and dO, three launches per step), counted as 2.5x the forward's FLOPs (five
+GEMM-shaped products against the forward's two); its CPU baseline is the fp64
+backward oracle on one (batch, head) at a reduced N.
+
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 on its own GPU (the forward pass shards into independent (batch, head)
 problems, so there is no data-path collective); rank 0 reports the units of
@@ -34,6 +39,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 and % of dense bf16 tensor peak at N=16K, d=128"
+METRIC_BWD = "attention bwd TFLOP/s on 1 GB300 (2.5x forward FLOPs) and % of dense bf16 tensor peak"
+BWD_FLOP_FACTOR = 2.5
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
@@ -51,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer end-to-end leg")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-baseline sample")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default, the headline metric) or the backward")
     return ap.parse_args(argv)
 
 
@@ -240,6 +249,119 @@ def workload_config(w, l2_note):
             "l2": l2_note, "parallelism": "replicas"}
 
 
+def cpu_oracle_bwd_sample(w, target_seconds: float):
+    """Time the fp64 backward oracle on one (batch, head) of workload `w` at a
+    reduced N chosen to take about `target_seconds`. Returns (TFLOP/s, seconds,
+    threads, description), FLOPs counted as the GPU's (2.5x the forward's)."""
+    import oracle
+    from exact_long_sequence_gb300 import workloads
+
+    oracle.build()
+    threads = os.cpu_count() or 1
+
+    def timed(n):
+        q, k, v = workloads.make_inputs(1, 1, n, w.d, w.seed, w.qk_dist, w.v_dist)
+        do = workloads.make_inputs(1, 1, n, w.d, w.seed + 1000)[0]
+        t0 = time.perf_counter()
+        oracle.attention_bwd(q, k, v, do, w.causal, w.scale, nthreads=threads)
+        return time.perf_counter() - t0
+
+    n = min(w.N, 512)
+    dt = timed(n)
+    while n < w.N and dt * 4 < target_seconds:  # cost grows as N^2
+        n, dt = min(w.N, 2 * n), None
+        dt = timed(n)
+    flops = BWD_FLOP_FACTOR * (2.0 if w.causal else 4.0) * n * n * w.d
+    desc = (f"full backward of one (batch, head) at N={n} (of {w.N}), d={w.d}, causal={w.causal}, fp64, "
+            f"{threads} threads; rate = {flops:.3g} FLOP / wall time")
+    return flops / dt / 1e12, dt, threads, desc
+
+
+def run_gb300_bwd(args, w):
+    import torch
+
+    import exact_long_sequence_gb300 as ela
+    from exact_long_sequence_gb300 import _build
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (sm_103a); no CPU fallback exists")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(ela.LIB_PATH):
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    ela.load_library()
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    q, k, v, do = (torch.randn(shape, device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
+    o, lse = ela.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, stream=stream)
+    ws = torch.empty(ela.load_library().attn_bwd_workspace_bytes(*shape), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        ela.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, workspace=ws, stream=stream)
+    torch.cuda.synchronize(dev)
+    if ela.last_device_error(stream) != ela.ATTN_OK:
+        raise SystemExit("kernel reported a device error during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            ela.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, workspace=ws, stream=stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    if ela.last_device_error(stream) != ela.ATTN_OK:
+        raise SystemExit("kernel reported a device error during the timed steps")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    slowest = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    flops = BWD_FLOP_FACTOR * w.flops
+    value = flops * args.steps * world / slowest / 1e12
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_sustained, peak_kind = read_peaks()
+    kernel_ms = statistics.mean(step_ms)
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                "peak_kind": f"{peak_kind} dense bf16 burst (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                else "fallback dense bf16 burst",
+                "traffic": None, "algorithmic_flops_per_launch": flops, "kernel_ms": kernel_ms,
+                "note": "step = the three launches of attn_bwd (row statistics, gradients, dQ to bf16)"}
+    if peak_sustained:
+        roofline["frac_of_sustained"] = achieved / peak_sustained
+    line = {
+        "metric": METRIC_BWD, "pass": "bwd", "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": slowest * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"),
+        "roofline": roofline, "gpu_launches": 3 * args.steps, "clocks": clocks.summary(),
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+        "e2e": None,
+    }
+    if not args.skip_cpu and world == 1:
+        v_cpu, dt, threads, desc = cpu_oracle_bwd_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+                                "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_gb300(args, w):
     import torch
 
@@ -381,6 +503,8 @@ def main(argv=None):
     w = workloads.WORKLOADS[name]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.which == "bwd":
+        return run_gb300_bwd(args, w)
     return run_gb300(args, w)
 
 
