@@ -66,9 +66,8 @@ WORKLOADS = {
 HEADLINE = "b1h16n16384d128"
 
 
-def make_inputs(B: int, H: int, N: int, d: int, seed: int, qk_dist: str = "normal",
-                v_dist: str = "normal"):
-    """Return bf16 CPU tensors (Q, K, V), each [B, H, N, d], by the recipe above."""
+def _draw(B: int, H: int, N: int, d: int, seed: int, qk_dist: str, v_dist: str):
+    """The fp32 draws of the recipe above, before any rounding."""
     g = torch.Generator("cpu").manual_seed(seed)
     shape = (B, H, N, d)
     q = torch.randn(shape, generator=g)
@@ -86,7 +85,36 @@ def make_inputs(B: int, H: int, N: int, d: int, seed: int, qk_dist: str = "norma
         k[mk] *= 10
     elif qk_dist != "normal":
         raise ValueError(qk_dist)
+    return q, k, v
+
+
+def make_inputs(B: int, H: int, N: int, d: int, seed: int, qk_dist: str = "normal",
+                v_dist: str = "normal"):
+    """Return bf16 CPU tensors (Q, K, V), each [B, H, N, d], by the recipe above."""
+    q, k, v = _draw(B, H, N, d, seed, qk_dist, v_dist)
     return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+E4M3_MAX = 448.0  # largest finite E4M3 value
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor E4M3 quantisation of an fp32 tensor: (codes as uint8, scale) with
+    scale = max|x| / 448, so that x ~= scale * e4m3(codes).  Rounding is torch's
+    float8_e4m3fn conversion (round to nearest even, saturating at 448)."""
+    amax = float(x.abs().max())
+    scale = amax / E4M3_MAX if amax > 0 else 1.0
+    codes = (x / scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.contiguous(), scale
+
+
+def make_inputs_fp8(B: int, H: int, N: int, d: int, seed: int, qk_dist: str = "normal",
+                    v_dist: str = "normal"):
+    """The same draws as make_inputs, quantised per tensor to E4M3: returns
+    (q8, k8, v8, (q_scale, k_scale, v_scale)) with uint8 code tensors [B, H, N, d]."""
+    q, k, v = _draw(B, H, N, d, seed, qk_dist, v_dist)
+    (q8, sq), (k8, sk), (v8, sv) = (quantize_e4m3(t) for t in (q, k, v))
+    return q8, k8, v8, (sq, sk, sv)
 
 
 def workload_inputs(w: Workload):

@@ -52,6 +52,10 @@ def _open(path: str):
     lib.oracle_attn_f64.restype = ctypes.c_int
     lib.oracle_attn_f64.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64] * 3 + [ctypes.c_int, ctypes.c_double,
                                                                                      ctypes.c_void_p, ctypes.c_void_p]
+    lib.oracle_attn_rows_f64.restype = ctypes.c_int
+    lib.oracle_attn_rows_f64.argtypes = lib.oracle_attn_rows.argtypes
+    lib.oracle_decode_e4m3.restype = ctypes.c_int
+    lib.oracle_decode_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]
     lib.oracle_attn_bwd_f64.restype = ctypes.c_int
     lib.oracle_attn_bwd_f64.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3 + [ctypes.c_int, ctypes.c_double]
                                         + [ctypes.c_void_p] * 3 + [ctypes.c_int])
@@ -138,6 +142,54 @@ def attention_f64(q, k, v, causal: bool, scale: float, _lib_handle=None):
     return O, LSE
 
 
+def attention_rows_f64(q, k, v, causal: bool, scale: float, rows=None, nthreads: int | None = None,
+                       return_probs: bool = False, _lib_handle=None):
+    """attention_rows on double inputs (float arrays are used as given)."""
+    qd, kd, vd = _as_f64(q), _as_f64(k), _as_f64(v)
+    N, d = qd.shape[-2], qd.shape[-1]
+    BH = int(np.prod(qd.shape[:-2]))
+    if rows is None:
+        R, rows_arr = N, None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(BH, -1))
+        R = rows_arr.shape[1]
+    O = np.empty((BH, R, d))
+    LSE = np.empty((BH, R))
+    P = np.empty((BH, R, N)) if return_probs else None
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    lib = _lib_handle if _lib_handle is not None else _load()
+    rc = lib.oracle_attn_rows_f64(qd.ctypes.data, kd.ctypes.data, vd.ctypes.data, BH, N, d, int(bool(causal)),
+                                  float(scale), rows_arr.ctypes.data if rows_arr is not None else None, R,
+                                  O.ctypes.data, LSE.ctypes.data, P.ctypes.data if P is not None else None,
+                                  int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_rows_f64 failed with status {rc}")
+    return (O, LSE, P) if return_probs else (O, LSE)
+
+
+def decode_e4m3(codes, scale: float = 1.0, _lib_handle=None) -> np.ndarray:
+    """scale * value of each E4M3 code (uint8 array or tensor), exactly, as float64."""
+    if not isinstance(codes, np.ndarray):
+        codes = codes.detach().to("cpu").contiguous().view(-1).numpy().view(np.uint8).reshape(tuple(codes.shape))
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib = _lib_handle if _lib_handle is not None else _load()
+    rc = lib.oracle_decode_e4m3(c.ctypes.data, c.size, float(scale), out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_decode_e4m3 failed with status {rc}")
+    return out
+
+
+def attention_fp8(q8, k8, v8, causal: bool, scale: float, scales=(1.0, 1.0, 1.0), rows=None,
+                  nthreads: int | None = None, return_probs: bool = False, _lib_handle=None):
+    """Forward for E4M3 inputs: Q = scales[0] * e4m3(q8), likewise K and V; then the
+    same graph as attention_rows on the decoded values."""
+    q, k, v = (decode_e4m3(x, s_, _lib_handle=_lib_handle) for x, s_ in zip((q8, k8, v8), scales))
+    return attention_rows_f64(q, k, v, causal, scale, rows=rows, nthreads=nthreads, return_probs=return_probs,
+                              _lib_handle=_lib_handle)
+
+
 def attention_bwd(q, k, v, do, causal: bool, scale: float, nthreads: int | None = None, _lib_handle=None):
     """Backward for upstream gradient dO: (dQ, dK, dV), each [BH, N, d] float64.
     bf16 tensors are decoded exactly; float arrays are used as given."""
@@ -171,3 +223,12 @@ class OracleBuild:
 
     def attention_bwd(self, *args, **kwargs):
         return attention_bwd(*args, _lib_handle=self._lib, **kwargs)
+
+    def attention_rows_f64(self, *args, **kwargs):
+        return attention_rows_f64(*args, _lib_handle=self._lib, **kwargs)
+
+    def decode_e4m3(self, *args, **kwargs):
+        return decode_e4m3(*args, _lib_handle=self._lib, **kwargs)
+
+    def attention_fp8(self, *args, **kwargs):
+        return attention_fp8(*args, _lib_handle=self._lib, **kwargs)

@@ -89,8 +89,13 @@ static void attend_one_row(const uint16_t *q, const uint16_t *Kh, const uint16_t
     *lse = m + log(l);
 }
 
+static void attend_one_row_f64(const double *q, const double *Kh, const double *Vh,
+                               int64_t N, int64_t d, int64_t i, int causal, double scale,
+                               double *s, double *o, double *lse);
+
 typedef struct {
     const uint16_t *Q, *K, *V;
+    const double *Qd, *Kd, *Vd; /* double inputs instead of Q, K, V when non-NULL */
     int64_t BH, N, d, R;
     int causal;
     double scale;
@@ -112,14 +117,65 @@ static void *oracle_worker(void *arg)
         int64_t i = job->rows ? job->rows[w] : r;
         if (i < 0 || i >= job->N) { job->status = 1; break; }
         const int64_t head = bh * job->N * job->d;
-        attend_one_row(job->Q + head + i * job->d, job->K + head, job->V + head,
-                       job->N, job->d, i, job->causal, job->scale, s,
-                       job->O + w * job->d, job->LSE + w);
+        if (job->Qd)
+            attend_one_row_f64(job->Qd + head + i * job->d, job->Kd + head, job->Vd + head,
+                               job->N, job->d, i, job->causal, job->scale, s,
+                               job->O + w * job->d, job->LSE + w);
+        else
+            attend_one_row(job->Q + head + i * job->d, job->K + head, job->V + head,
+                           job->N, job->d, i, job->causal, job->scale, s,
+                           job->O + w * job->d, job->LSE + w);
         if (job->P)
             memcpy(job->P + w * job->N, s, sizeof(double) * (size_t)job->N);
     }
     free(s);
     return NULL;
+}
+
+/*
+ * Attention forward for selected query rows, fp64, threaded over rows.
+ *   Q, K, V   : [BH, N, d] bf16 bit patterns
+ *   rows      : [BH, R] query positions per (batch, head), or NULL meaning
+ *               R == N and every row in order
+ *   O, LSE, P : outputs as above (P may be NULL)
+ *   nthreads  : worker threads (>= 1)
+ * Returns 0, or 1 for a bad argument / row index, 2 for out of memory.
+ */
+/* Runs the row jobs of one call on `nthreads` threads; `proto` holds the
+ * inputs and outputs, the work range is filled in here. */
+static int run_row_jobs(const oracle_job *proto, int nthreads)
+{
+    const int64_t items = proto->BH * proto->R;
+    if (items == 0)
+        return 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > items) nthreads = (int)items;
+    oracle_job *jobs = (oracle_job *)calloc((size_t)nthreads, sizeof(oracle_job));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(jobs); free(tids); return 2; }
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *proto;
+        jobs[t].first = items * t / nthreads;
+        jobs[t].last = items * (t + 1) / nthreads;
+        jobs[t].status = 0;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, oracle_worker, &jobs[t]) != 0) break;
+        started = t;
+    }
+    oracle_worker(&jobs[0]);
+    /* Threads that failed to start: run their share here. */
+    for (int t = started + 1; t < nthreads; ++t)
+        oracle_worker(&jobs[t]);
+    int status = jobs[0].status;
+    for (int t = 1; t <= started; ++t)
+        pthread_join(tids[t], NULL);
+    for (int t = 1; t < nthreads; ++t)
+        if (jobs[t].status) status = jobs[t].status;
+    free(jobs);
+    free(tids);
+    return status;
 }
 
 /*
@@ -140,36 +196,56 @@ int oracle_attn_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
         return 1;
     if (!rows && R != N)
         return 1;
-    const int64_t items = BH * R;
-    if (items == 0)
-        return 0;
-    if (nthreads < 1) nthreads = 1;
-    if (nthreads > items) nthreads = (int)items;
-    oracle_job *jobs = (oracle_job *)calloc((size_t)nthreads, sizeof(oracle_job));
-    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
-    if (!jobs || !tids) { free(jobs); free(tids); return 2; }
-    for (int t = 0; t < nthreads; ++t) {
-        oracle_job j = {Q, K, V, BH, N, d, R, causal, scale, rows, O, LSE, P,
-                        items * t / nthreads, items * (t + 1) / nthreads, 0};
-        jobs[t] = j;
-    }
-    int started = 0;
-    for (int t = 1; t < nthreads; ++t) {
-        if (pthread_create(&tids[t], NULL, oracle_worker, &jobs[t]) != 0) break;
-        started = t;
-    }
-    oracle_worker(&jobs[0]);
-    /* Threads that failed to start: run their share here. */
-    for (int t = started + 1; t < nthreads; ++t)
-        oracle_worker(&jobs[t]);
-    int status = jobs[0].status;
-    for (int t = 1; t <= started; ++t)
-        pthread_join(tids[t], NULL);
-    for (int t = 1; t < nthreads; ++t)
-        if (jobs[t].status) status = jobs[t].status;
-    free(jobs);
-    free(tids);
-    return status;
+    oracle_job j = {Q, K, V, NULL, NULL, NULL, BH, N, d, R, causal, scale, rows, O, LSE, P, 0, 0, 0};
+    return run_row_jobs(&j, nthreads);
+}
+
+/* The same on double-precision inputs Q, K, V [BH, N, d]. */
+int oracle_attn_rows_f64(const double *Q, const double *K, const double *V,
+                         int64_t BH, int64_t N, int64_t d, int causal, double scale,
+                         const int64_t *rows, int64_t R,
+                         double *O, double *LSE, double *P, int nthreads)
+{
+    if (!Q || !K || !V || !O || !LSE || BH < 0 || N < 1 || d < 1 || R < 0)
+        return 1;
+    if (!rows && R != N)
+        return 1;
+    oracle_job j = {NULL, NULL, NULL, Q, K, V, BH, N, d, R, causal, scale, rows, O, LSE, P, 0, 0, 0};
+    return run_row_jobs(&j, nthreads);
+}
+
+/* ------------------------------------------------------------------------
+ * 8-bit floating-point inputs.
+ *
+ * The FP8 forward takes Q, K, V as E4M3 codes with one fp32 scale per tensor:
+ * the value of code c of tensor X is scale_X * e4m3(c).  E4M3 is the 8-bit
+ * format of the OCP 8-bit Floating Point specification (OFP8): 1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the
+ * subnormals m/8 * 2^-6; the code S.1111.111 is NaN; there are no infinities
+ * (the largest finite value is 1.75 * 2^8 = 448).  The oracle decodes every
+ * code exactly to double, applies the scale, and runs the same attention
+ * graph on the decoded values.
+ * ------------------------------------------------------------------------ */
+static double e4m3_to_double(uint8_t code)
+{
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* dst[i] = scale * e4m3(src[i]) for i < n. */
+int oracle_decode_e4m3(const uint8_t *src, int64_t n, double scale, double *dst)
+{
+    if ((!src || !dst) && n > 0) return 1;
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = scale * e4m3_to_double(src[i]);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------

@@ -119,3 +119,50 @@ def test_backward_pins_catch_planted_mistake(tmp_path, mutation):
         except (AssertionError, ValueError, FloatingPointError):
             caught.append(name)
     assert caught, f"no backward pin caught mutation {mutation}"
+
+
+FP8_MUTATIONS = {
+    "e4m3_bias_8": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "e4m3_no_implicit_one": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp((double)m / 8.0, e - 7);"),
+    "e4m3_subnormal_exponent": ("v = ldexp((double)m / 8.0, -6);", "v = ldexp((double)m / 8.0, -7);"),
+    "e4m3_sign_dropped": ("return sign ? -v : v;", "return v;"),
+    "e4m3_nan_not_decoded": ("if (e == 15 && m == 7)\n        return NAN;", "if (e == 16)\n        return NAN;"),
+    "e4m3_scale_dropped": ("dst[i] = scale * e4m3_to_double(src[i]);", "dst[i] = e4m3_to_double(src[i]);"),
+}
+
+
+def _module_pins(modname):
+    import importlib
+
+    mod = importlib.import_module(modname)
+    out = []
+    for name, fn in inspect.getmembers(mod, inspect.isfunction):
+        if not name.startswith("test_") or "oracle_mod" not in inspect.signature(fn).parameters:
+            continue
+        grid = [{}]
+        for m in getattr(fn, "pytestmark", []):
+            if m.name == "parametrize":
+                names = [n.strip() for n in m.args[0].split(",")]
+                grid = [{**g, **dict(zip(names, val if len(names) > 1 else (val,)))} for g in grid for val in m.args[1]]
+        out += [(name, fn, kw) for kw in grid]
+    return out
+
+
+@pytest.mark.parametrize("mutation", sorted(FP8_MUTATIONS))
+def test_fp8_pins_catch_planted_mistake(tmp_path, mutation):
+    old, new = FP8_MUTATIONS[mutation]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found exactly once: {old!r}"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    str(mutant_c), "-o", str(lib), "-lm"], check=True)
+    mutant = oracle.OracleBuild(str(lib))
+    caught = []
+    for name, fn, kw in _module_pins("test_oracle_fp8"):
+        try:
+            fn(mutant, **kw)
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(name)
+    assert caught, f"no FP8 pin caught mutation {mutation}"
