@@ -13,6 +13,11 @@ the events. `e2e` times the same pass through the host-buffer C-ABI entry
 `--impl reference` times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of query rows of the same workload.
 
+`--fp8` times the FP8 forward (attn_fwd_fp8: E4M3 Q, K, V with per-tensor
+scales; two launches per step, the transpose of V and the attention kernel)
+against the FP8 peak, taken as the measured bf16 peak times the nominal FP8 /
+BF16 ratio of 2.
+
 `--pass bwd` times the backward instead (attn_bwd: dQ, dK, dV from Q, K, V, O,
 LSE and dO, three launches per step), counted as 2.5x the forward's FLOPs (five
 GEMM-shaped products against the forward's two); its CPU baseline is the fp64
@@ -58,6 +63,7 @@ def parse_args(argv=None):
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer end-to-end leg")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-baseline sample")
+    ap.add_argument("--fp8", action="store_true", help="time the FP8 (E4M3) forward instead of the bf16 one")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default, the headline metric) or the backward")
     return ap.parse_args(argv)
@@ -275,6 +281,138 @@ def cpu_oracle_bwd_sample(w, target_seconds: float):
     desc = (f"full backward of one (batch, head) at N={n} (of {w.N}), d={w.d}, causal={w.causal}, fp64, "
             f"{threads} threads; rate = {flops:.3g} FLOP / wall time")
     return flops / dt / 1e12, dt, threads, desc
+
+
+def cpu_oracle_fp8_sample(w, target_seconds: float, seed: int = 0):
+    """Time the fp64 oracle of the FP8 forward (decode + forward) on sampled query rows
+    of one (batch, head) of workload `w`. Returns (TFLOP/s, seconds, rows, threads, description)."""
+    import oracle
+    from exact_long_sequence_gb300 import workloads
+
+    oracle.build()
+    threads = os.cpu_count() or 1
+    q8, k8, v8, sc = workloads.make_inputs_fp8(1, 1, w.N, w.d, w.seed, w.qk_dist, w.v_dist)
+    flops_per_row = (2.0 if w.causal else 4.0) * w.N * w.d
+
+    def timed(rows):
+        r = workloads.sample_rows(1, w.N, rows, seed + w.seed).numpy()
+        t0 = time.perf_counter()
+        oracle.attention_fp8(q8, k8, v8, w.causal, w.scale, scales=sc, rows=r, nthreads=threads)
+        return time.perf_counter() - t0, r.shape[1]
+
+    probe_rows = max(threads, 32)
+    dt, n = timed(probe_rows)
+    rows = int(min(w.N, max(probe_rows, probe_rows * target_seconds / max(dt, 1e-6))))
+    dt, n = timed(rows)
+    desc = (f"{n} random query rows of one (batch, head) of {w.name} in E4M3 (N={w.N}, d={w.d}, "
+            f"causal={w.causal}), decoded exactly, fp64, {threads} threads")
+    return flops_per_row * n / dt / 1e12, dt, n, threads, desc
+
+
+def run_gb300_fp8(args, w):
+    import torch
+
+    import exact_long_sequence_gb300 as ela
+    from exact_long_sequence_gb300 import _build
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (sm_103a); no CPU fallback exists")
+    if w.d != 128:
+        raise SystemExit("the FP8 forward supports d = 128 only")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(ela.LIB_PATH):
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    ela.load_library()
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    # Device-resident synthetic inputs with the workload's distributions, quantised per tensor to E4M3
+    # (scale = max|x| / 448).
+    xs = [torch.randn(shape, device=dev, generator=g) for _ in range(2)]
+    xs.append(torch.randn(shape, device=dev, generator=g) if w.v_dist == "normal"
+              else torch.rand(shape, device=dev, generator=g) * 2 - 1)
+    if w.qk_dist == "normal_spiky":
+        for i in range(2):
+            xs[i] = torch.where(torch.rand(shape, device=dev, generator=g) < 0.01, xs[i] * 10, xs[i])
+    codes, scales = [], []
+    for x in xs:
+        sc = float(x.abs().max()) / 448.0
+        codes.append((x / sc).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).contiguous())
+        scales.append(sc)
+    del xs
+    q8, k8, v8 = codes
+    o = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
+    ws = torch.empty(ela.load_library().attn_fwd_fp8_workspace_bytes(*shape), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        ela.attn_fwd_fp8(q8, k8, v8, scales, causal=w.causal, scale=w.scale, out=o, lse=lse, workspace=ws,
+                         stream=stream)
+    torch.cuda.synchronize(dev)
+    if ela.last_device_error(stream) != ela.ATTN_OK:
+        raise SystemExit("kernel reported a device error during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            ela.attn_fwd_fp8(q8, k8, v8, scales, causal=w.causal, scale=w.scale, out=o, lse=lse, workspace=ws,
+                             stream=stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    if ela.last_device_error(stream) != ela.ATTN_OK:
+        raise SystemExit("kernel reported a device error during the timed steps")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    slowest = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    value = w.flops * args.steps * world / slowest / 1e12
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peak_bf16, peak_bf16_sustained, peak_kind = read_peaks()
+    peak = 2.0 * peak_bf16
+    kernel_ms = statistics.mean(step_ms)
+    achieved = w.flops / (kernel_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                "peak_kind": (f"{peak_kind} dense bf16 burst (MEASURED_PEAKS.json) x 2, the nominal FP8/BF16 "
+                              "tensor ratio (4.5 / 2.25 PFLOP/s)"),
+                "traffic": None, "algorithmic_flops_per_launch": w.flops, "kernel_ms": kernel_ms,
+                "note": "step = the V transpose and the attention kernel; the step time is used for both",
+                "frac_of_bf16_peak": achieved / peak_bf16}
+    if peak_bf16_sustained:
+        roofline["frac_of_sustained"] = achieved / (2.0 * peak_bf16_sustained)
+    line = {
+        "metric": METRIC + " (FP8 E4M3 inputs)", "precision": "e4m3", "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": slowest * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": workload_config(w, f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"),
+        "roofline": roofline, "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+        "e2e": None,
+    }
+    line["config"]["inputs"] = f"seeded synthetic ({w.qk_dist} Q,K; {w.v_dist} V), E4M3 per-tensor amax scaling"
+    if not args.skip_cpu and world == 1:
+        v_cpu, dt, rows, threads, desc = cpu_oracle_fp8_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+                                "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
 
 
 def run_gb300_bwd(args, w):
@@ -505,6 +643,8 @@ def main(argv=None):
         return run_reference(args, w)
     if args.which == "bwd":
         return run_gb300_bwd(args, w)
+    if args.fp8:
+        return run_gb300_fp8(args, w)
     return run_gb300(args, w)
 
 

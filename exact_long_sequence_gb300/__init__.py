@@ -44,6 +44,8 @@ EXPORTED_SYMBOLS = (
     "attn_fwd_noalloc",
     "attn_bwd",
     "attn_bwd_workspace_bytes",
+    "attn_fwd_fp8",
+    "attn_fwd_fp8_workspace_bytes",
 )
 
 
@@ -107,6 +109,10 @@ def load_library(path: str | None = None):
     lib.attn_bwd.restype = i
     lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_fwd_fp8.argtypes = [vp] * 5 + [i, i, i, i, i, f, f, f, f, vp, ctypes.c_size_t, vp]
+    lib.attn_fwd_fp8.restype = i
+    lib.attn_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
+    lib.attn_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
     if path is None:
         _lib = lib
     return lib
@@ -191,6 +197,36 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
                           workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_fwd_fp8(q8, k8, v8, scales, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                 workspace=None, stream=None):
+    """FP8 forward: q8, k8, v8 are uint8 CUDA tensors [B, H, N, d] of E4M3 codes and
+    `scales` = (q_scale, k_scale, v_scale), the real inputs being scale * e4m3(code).
+    Returns (o bf16 [B, H, N, d], lse fp32 [B, H, N]).  d must be 128."""
+    import torch
+
+    lib = load_library()
+    for t in (q8, k8, v8):
+        if t.shape != q8.shape or t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q8, k8, v8 must be contiguous uint8 (E4M3 code) CUDA tensors of one [B, H, N, d] shape")
+    B, H, N, d = q8.shape
+    if scale is None:
+        scale = default_scale(d)
+    if out is None:
+        out = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    need = lib.attn_fwd_fp8_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q8.device)
+    sq, sk, sv = (float(x) for x in scales)
+    with torch.cuda.device(q8.device):
+        st = lib.attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, d,
+                              int(bool(causal)), float(scale), sq, sk, sv, workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "attn_fwd_fp8")
+    return out, lse
 
 
 def attn_fwd_noalloc(q, k, v, out, lse, causal: bool = False, scale: float | None = None, stream=None):

@@ -92,6 +92,19 @@ int encode_f32_rows_map(CUtensorMap* map, void* base, int BH, int N, int d, int 
     return ATTN_OK;
 }
 
+int encode_u8_map(CUtensorMap* map, const void* base, uint64_t e0, uint64_t e1, uint64_t e2, uint64_t s1,
+                  uint64_t s2, uint32_t b0, uint32_t b1) {
+    cuuint64_t dims[3] = {e0, e1, e2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+    return ATTN_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_args(const void* Q, const void* K, const void* V, const void* O, const void* LSE, int B, int H, int N,

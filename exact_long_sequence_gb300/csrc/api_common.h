@@ -21,6 +21,7 @@ struct DeviceState {
     uint32_t* error_word = nullptr;  // 256-byte device block, first word = error code
     bool smem_configured[2][2] = {{false, false}, {false, false}};      // forward <d == 128><causal>
     bool bwd_smem_configured[2][2] = {{false, false}, {false, false}};  // backward <d == 128><causal>
+    bool fp8_smem_configured[2] = {false, false};                         // FP8 forward <causal>
 };
 
 // The cudaError_t of this thread's most recent ATTN_ERR_CUDA.
@@ -44,6 +45,12 @@ int encode_rows_map(CUtensorMap* map, const void* base, int BH, int N, int d, in
 // An fp32 tensor viewed as [BH][N][d], written by TMA (reduce-add) in boxes of
 // d columns x box_rows rows, unswizzled.  Rows past N are dropped.
 int encode_f32_rows_map(CUtensorMap* map, void* base, int BH, int N, int d, int box_rows);
+
+// A 3-D byte tensor (E4M3 codes) with extents {e0, e1, e2} (e0 innermost) and
+// byte strides s1, s2 (multiples of 16), read by TMA in boxes of b0 x b1 with
+// the 128-byte swizzle (b0 = 128).  Elements past an extent read as zero.
+int encode_u8_map(CUtensorMap* map, const void* base, uint64_t e0, uint64_t e1, uint64_t e2, uint64_t s1,
+                  uint64_t s2, uint32_t b0, uint32_t b1);
 
 bool aligned16(const void* p);
 

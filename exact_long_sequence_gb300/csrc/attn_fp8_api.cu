@@ -1,0 +1,136 @@
+// C ABI of the FP8 (E4M3) exact-attention forward: argument checks, the
+// transposed copy of V, TMA descriptors and the launch of the FP8
+// instantiation of the forward kernel.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/exact_attn.h"
+#include "api_common.h"
+#include "attn_fwd_kernel.cuh"
+#include "plan.h"
+
+extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out);
+
+namespace elsattn {
+namespace {
+
+constexpr int kFp8D = 128;  // the E4M3 tiles are one 128-byte swizzle row wide
+
+// Row pitch (bytes) of the transposed V: a multiple of 16, as TMA strides must be.
+size_t vt_pitch(int N) { return (static_cast<size_t>(N) + 15) / 16 * 16; }
+
+// Vt[bh][c][j] = V[bh][j][c] for one (batch, head) and one tile of 128 keys,
+// through a padded shared-memory tile.  Keys past N are written as zero up to
+// the padded pitch.
+__global__ void __launch_bounds__(256) transpose_v_e4m3(const uint8_t* V, uint8_t* Vt, int N, size_t pitch) {
+    __shared__ __align__(16) uint8_t tile[128][kFp8D + 4];
+    const int bh = blockIdx.y;
+    const int j0 = blockIdx.x * 128;
+    const uint8_t* src = V + static_cast<size_t>(bh) * N * kFp8D;
+    for (int i = threadIdx.x; i < 128 * (kFp8D / 16); i += blockDim.x) {
+        const int r = i / (kFp8D / 16), c16 = (i % (kFp8D / 16)) * 16;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (j0 + r < N) v = *reinterpret_cast<const uint4*>(src + static_cast<size_t>(j0 + r) * kFp8D + c16);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&tile[r][c16]);
+        dst[0] = v.x;
+        dst[1] = v.y;
+        dst[2] = v.z;
+        dst[3] = v.w;
+    }
+    __syncthreads();
+    uint8_t* out = Vt + static_cast<size_t>(bh) * kFp8D * pitch;
+    for (int i = threadIdx.x; i < kFp8D * 8; i += blockDim.x) {
+        const int c = i / 8, k16 = (i % 8) * 16;
+        if (j0 + k16 >= N) continue;
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            w[q] = static_cast<uint32_t>(tile[k16 + 4 * q][c]) | (static_cast<uint32_t>(tile[k16 + 4 * q + 1][c]) << 8) |
+                   (static_cast<uint32_t>(tile[k16 + 4 * q + 2][c]) << 16) |
+                   (static_cast<uint32_t>(tile[k16 + 4 * q + 3][c]) << 24);
+        *reinterpret_cast<uint4*>(out + static_cast<size_t>(c) * pitch + j0 + k16) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <bool CAUSAL>
+int launch_fp8(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, const CUtensorMap& tk,
+               const CUtensorMap& tvt, const FwdParams& p, cudaStream_t stream) {
+    auto kernel = attn_fwd_kernel<kFp8D, CAUSAL, true>;
+    constexpr int smem = smem_bytes_for(kFp8D, 1);
+    bool& configured = dev.fp8_smem_configured[CAUSAL];
+    cudaError_t e;
+    if (!configured) {
+        if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return cuda_fail(e);
+        configured = true;
+    }
+    kernel<<<plan.grid, plan.threads, smem, stream>>>(tq, tk, tvt, p);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+bool positive_finite(float x) { return std::isfinite(x) && x > 0.f; }
+
+}  // namespace
+}  // namespace elsattn
+
+using namespace elsattn;
+
+extern "C" size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+    return static_cast<size_t>(B) * H * d * vt_pitch(N);
+}
+
+extern "C" int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void* O, float* LSE, int B, int H, int N,
+                            int d, int causal, float scale, float q_scale, float k_scale, float v_scale,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    int st = check_args(Q8, K8, V8, O, LSE, B, H, N, d, scale);
+    if (st != ATTN_OK) return st;
+    if (!positive_finite(q_scale) || !positive_finite(k_scale) || !positive_finite(v_scale))
+        return ATTN_ERR_INVALID_ARG;
+    if (d != kFp8D) return ATTN_ERR_UNSUPPORTED;
+    if (!workspace) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+    if (workspace_bytes < attn_fwd_fp8_workspace_bytes(B, H, N, d)) return ATTN_ERR_INVALID_ARG;
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    attn_plan_t plan;
+    if ((st = attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan)) != ATTN_OK) return st;
+
+    const int BH = B * H;
+    const size_t pitch = vt_pitch(N);
+    uint8_t* vt = static_cast<uint8_t*>(workspace);
+    {
+        const dim3 grid((N + 127) / 128, BH);
+        transpose_v_e4m3<<<grid, 256, 0, stream>>>(static_cast<const uint8_t*>(V8), vt, N, pitch);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    CUtensorMap tq, tk, tvt;
+    const uint64_t rows = static_cast<uint64_t>(N), bh = static_cast<uint64_t>(BH);
+    if ((st = encode_u8_map(&tq, Q8, kFp8D, rows, bh, kFp8D, rows * kFp8D, kFp8D, kBr)) != ATTN_OK ||
+        (st = encode_u8_map(&tk, K8, kFp8D, rows, bh, kFp8D, rows * kFp8D, kFp8D, kBc)) != ATTN_OK ||
+        (st = encode_u8_map(&tvt, vt, rows, kFp8D, bh, pitch, pitch * kFp8D, kBc, kFp8D)) != ATTN_OK)
+        return st;
+
+    FwdParams p;
+    p.O = static_cast<__nv_bfloat16*>(O);
+    p.LSE = LSE;
+    p.error_word = dev->error_word;
+    p.timeout_ns = kDefaultTimeoutNs;
+    p.N = N;
+    p.BH = BH;
+    p.num_q_tiles = (N + kBr - 1) / kBr;
+    p.num_kv_tiles = (N + kBc - 1) / kBc;
+    p.num_pairs = (p.num_q_tiles + 1) / 2;
+    p.num_units = plan.num_units;
+    p.heads_per_group = plan.heads_per_group;
+    p.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+    p.out_scale = v_scale;
+    return causal ? launch_fp8<true>(*dev, plan, tq, tk, tvt, p, stream)
+                  : launch_fp8<false>(*dev, plan, tq, tk, tvt, p, stream);
+}

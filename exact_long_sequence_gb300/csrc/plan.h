@@ -21,26 +21,30 @@ constexpr int kSmemAlign = 1024;    // slack to align the tiles to the 1024-byte
 constexpr int kFixedBarriers = 15;  // mbarriers besides the two per K/V stage
 constexpr int kFlagBytes = 16;      // TMEM base address slot and abort flag
 
-// Bytes of one [128 x d] bf16 tile (Q, K and V tiles all have this size since kBr == kBc).
-constexpr int tile_bytes(int d) { return kBr * d * 2; }
+// Bytes of one [128 x d] tile of `esize`-byte elements (Q, K and V tiles all
+// have this size since kBr == kBc): bf16 (esize 2) by default, E4M3 (esize 1)
+// for the FP8 forward.
+constexpr int tile_bytes(int d, int esize = 2) { return kBr * d * esize; }
 
 // Bytes besides the tiles: alignment slack, mbarriers, flags.
 constexpr int overhead_bytes(int stages) { return kSmemAlign + (2 * stages + kFixedBarriers) * 8 + kFlagBytes; }
 
 // Deepest K/V ring that fits next to the resident query tiles, capped at 8.
-constexpr int kv_stages_for(int d) {
-    return ((kSmemLimit - overhead_bytes(0) - kQTiles * tile_bytes(d)) / (tile_bytes(d) + 16)) > 8
+constexpr int kv_stages_for(int d, int esize = 2) {
+    return ((kSmemLimit - overhead_bytes(0) - kQTiles * tile_bytes(d, esize)) / (tile_bytes(d, esize) + 16)) > 8
                ? 8
-               : ((kSmemLimit - overhead_bytes(0) - kQTiles * tile_bytes(d)) / (tile_bytes(d) + 16));
+               : ((kSmemLimit - overhead_bytes(0) - kQTiles * tile_bytes(d, esize)) / (tile_bytes(d, esize) + 16));
 }
 
-constexpr int smem_bytes_for(int d) {
-    return overhead_bytes(kv_stages_for(d)) + kQTiles * tile_bytes(d) + kv_stages_for(d) * tile_bytes(d);
+constexpr int smem_bytes_for(int d, int esize = 2) {
+    return overhead_bytes(kv_stages_for(d, esize)) + kQTiles * tile_bytes(d, esize) +
+           kv_stages_for(d, esize) * tile_bytes(d, esize);
 }
 
 static_assert(kv_stages_for(128) >= 3, "d=128 ring too shallow");
 static_assert(smem_bytes_for(128) <= kSmemLimit && smem_bytes_for(64) <= kSmemLimit, "smem");
 // Two CTAs must never share an SM (each allocates all 512 TMEM columns).
 static_assert(2 * smem_bytes_for(64) > 233472 && 2 * smem_bytes_for(128) > 233472, "1 CTA/SM");
+static_assert(2 * smem_bytes_for(128, 1) > 233472, "1 CTA/SM (E4M3)");
 
 }  // namespace elsattn
