@@ -56,6 +56,11 @@ def _open(path: str):
     lib.oracle_attn_rows_f64.argtypes = lib.oracle_attn_rows.argtypes
     lib.oracle_decode_e4m3.restype = ctypes.c_int
     lib.oracle_decode_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]
+    lib.oracle_softmax_rows.restype = ctypes.c_int
+    lib.oracle_softmax_rows.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    lib.oracle_layernorm_rows.restype = ctypes.c_int
+    lib.oracle_layernorm_rows.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int64, ctypes.c_int64, ctypes.c_double,
+                                                                   ctypes.c_void_p]
     lib.oracle_attn_bwd_f64.restype = ctypes.c_int
     lib.oracle_attn_bwd_f64.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3 + [ctypes.c_int, ctypes.c_double]
                                         + [ctypes.c_void_p] * 3 + [ctypes.c_int])
@@ -190,6 +195,34 @@ def attention_fp8(q8, k8, v8, causal: bool, scale: float, scales=(1.0, 1.0, 1.0)
                               _lib_handle=_lib_handle)
 
 
+def softmax_rows(x, _lib_handle=None) -> np.ndarray:
+    """Row softmax over the last axis (bf16 tensors decoded exactly; float arrays as given)."""
+    xd = _as_f64(x)
+    N = xd.shape[-1]
+    R = xd.size // N
+    y = np.empty(xd.shape)
+    lib = _lib_handle if _lib_handle is not None else _load()
+    rc = lib.oracle_softmax_rows(xd.ctypes.data, R, N, y.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_softmax_rows failed with status {rc}")
+    return y
+
+
+def layernorm_rows(x, gamma, beta, eps: float, _lib_handle=None) -> np.ndarray:
+    """Layer normalisation over the last axis with per-column gamma, beta."""
+    xd, gd, bd = _as_f64(x), _as_f64(gamma), _as_f64(beta)
+    N = xd.shape[-1]
+    R = xd.size // N
+    if gd.shape != (N,) or bd.shape != (N,):
+        raise ValueError("gamma and beta must have the row length")
+    y = np.empty(xd.shape)
+    lib = _lib_handle if _lib_handle is not None else _load()
+    rc = lib.oracle_layernorm_rows(xd.ctypes.data, gd.ctypes.data, bd.ctypes.data, R, N, float(eps), y.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_layernorm_rows failed with status {rc}")
+    return y
+
+
 def attention_bwd(q, k, v, do, causal: bool, scale: float, nthreads: int | None = None, _lib_handle=None):
     """Backward for upstream gradient dO: (dQ, dK, dV), each [BH, N, d] float64.
     bf16 tensors are decoded exactly; float arrays are used as given."""
@@ -232,3 +265,9 @@ class OracleBuild:
 
     def attention_fp8(self, *args, **kwargs):
         return attention_fp8(*args, _lib_handle=self._lib, **kwargs)
+
+    def softmax_rows(self, *args, **kwargs):
+        return softmax_rows(*args, _lib_handle=self._lib, **kwargs)
+
+    def layernorm_rows(self, *args, **kwargs):
+        return layernorm_rows(*args, _lib_handle=self._lib, **kwargs)

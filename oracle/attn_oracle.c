@@ -415,3 +415,56 @@ int oracle_attn_bwd_f64(const double *Q, const double *K, const double *V, const
     free(tids);
     return status;
 }
+
+/* ------------------------------------------------------------------------
+ * Standalone row operations ("Softmax streaming" and "LayerNorm streaming" in
+ * the outlook of "From Attention Graph to FlashAttention - A Memory-Centric
+ * Compilation Approach in AICF", section 8).  The oracle computes each from its
+ * plain definition, row by row, in fp64.
+ * ------------------------------------------------------------------------ */
+
+/* Y[r, i] = exp(X[r, i] - max_j X[r, j]) / sum_j exp(X[r, j] - max_j X[r, j]). */
+int oracle_softmax_rows(const double *X, int64_t R, int64_t N, double *Y)
+{
+    if (!X || !Y || R < 0 || N < 1) return 1;
+    for (int64_t r = 0; r < R; ++r) {
+        const double *x = X + r * N;
+        double *y = Y + r * N;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j)
+            if (x[j] > m) m = x[j];
+        double l = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            y[j] = exp(x[j] - m);
+            l += y[j];
+        }
+        for (int64_t j = 0; j < N; ++j)
+            y[j] /= l;
+    }
+    return 0;
+}
+
+/* Layer normalisation of each row:
+ *   mean = sum_j x_j / N,  var = sum_j (x_j - mean)^2 / N  (the population variance),
+ *   Y[r, i] = (x_i - mean) / sqrt(var + eps) * gamma[i] + beta[i]. */
+int oracle_layernorm_rows(const double *X, const double *gamma, const double *beta, int64_t R, int64_t N,
+                          double eps, double *Y)
+{
+    if (!X || !gamma || !beta || !Y || R < 0 || N < 1 || !(eps >= 0.0)) return 1;
+    for (int64_t r = 0; r < R; ++r) {
+        const double *x = X + r * N;
+        double *y = Y + r * N;
+        double mean = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            mean += x[j];
+        mean /= (double)N;
+        double var = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            var += (x[j] - mean) * (x[j] - mean);
+        var /= (double)N;
+        const double rstd = 1.0 / sqrt(var + eps);
+        for (int64_t j = 0; j < N; ++j)
+            y[j] = (x[j] - mean) * rstd * gamma[j] + beta[j];
+    }
+    return 0;
+}

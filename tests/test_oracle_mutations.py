@@ -166,3 +166,36 @@ def test_fp8_pins_catch_planted_mistake(tmp_path, mutation):
         except (AssertionError, ValueError, FloatingPointError):
             caught.append(name)
     assert caught, f"no FP8 pin caught mutation {mutation}"
+
+
+ROWWISE_MUTATIONS = {
+    "softmax_no_max_subtraction": ("            y[j] = exp(x[j] - m);\n            l += y[j];",
+                                   "            y[j] = exp(x[j]);\n            l += y[j];"),
+    "softmax_not_normalised": ("        for (int64_t j = 0; j < N; ++j)\n            y[j] /= l;\n    }\n    return 0;\n}\n\n/* Layer",
+                               "        for (int64_t j = 0; j < N; ++j)\n            y[j] /= 1.0;\n    }\n    return 0;\n}\n\n/* Layer"),
+    "layernorm_unbiased_variance": ("        var /= (double)N;", "        var /= (double)(N > 1 ? N - 1 : 1);"),
+    "layernorm_eps_outside_sqrt": ("const double rstd = 1.0 / sqrt(var + eps);", "const double rstd = 1.0 / (sqrt(var) + eps);"),
+    "layernorm_gamma_beta_swapped": ("y[j] = (x[j] - mean) * rstd * gamma[j] + beta[j];",
+                                     "y[j] = (x[j] - mean) * rstd * beta[j] + gamma[j];"),
+    "layernorm_mean_not_removed": ("y[j] = (x[j] - mean) * rstd * gamma[j] + beta[j];", "y[j] = x[j] * rstd * gamma[j] + beta[j];"),
+}
+
+
+@pytest.mark.parametrize("mutation", sorted(ROWWISE_MUTATIONS))
+def test_rowwise_pins_catch_planted_mistake(tmp_path, mutation):
+    old, new = ROWWISE_MUTATIONS[mutation]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not found exactly once: {old!r}"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    str(mutant_c), "-o", str(lib), "-lm"], check=True)
+    mutant = oracle.OracleBuild(str(lib))
+    caught = []
+    for name, fn, kw in _module_pins("test_oracle_rowwise"):
+        try:
+            fn(mutant, **kw)
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(name)
+    assert caught, f"no row-operation pin caught mutation {mutation}"
