@@ -18,6 +18,11 @@ scales; two launches per step, the transpose of V and the attention kernel)
 against the FP8 peak, taken as the measured bf16 peak times the nominal FP8 /
 BF16 ratio of 2.
 
+`--pass softmax` and `--pass layernorm` time the standalone streaming row
+operations on their row workloads (`--workload` names one of
+workloads.ROW_WORKLOADS) in GB/s of one read and one write of every element,
+against the measured HBM copy bandwidth.
+
 `--pass bwd` times the backward instead (attn_bwd: dQ, dK, dV from Q, K, V, O,
 LSE and dO, three launches per step), counted as 2.5x the forward's FLOPs (five
 GEMM-shaped products against the forward's two); its CPU baseline is the fp64
@@ -64,8 +69,8 @@ def parse_args(argv=None):
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-baseline sample")
     ap.add_argument("--fp8", action="store_true", help="time the FP8 (E4M3) forward instead of the bf16 one")
-    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
-                    help="time the forward (default, the headline metric) or the backward")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "softmax", "layernorm"], default="fwd",
+                    help="time the forward (default, the headline metric), the backward, or a row operation")
     return ap.parse_args(argv)
 
 
@@ -415,6 +420,132 @@ def run_gb300_fp8(args, w):
     return 0
 
 
+def read_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def cpu_oracle_rows_sample(kind, N, target_seconds: float):
+    """Time the fp64 oracle of a row operation on whole rows of length N; returns
+    (GB/s of one bf16 read + write per element, seconds, rows, description)."""
+    import oracle
+    from exact_long_sequence_gb300 import workloads
+
+    oracle.build()
+
+    def timed(r):
+        inp = workloads.row_inputs(kind, r, N, seed=1)
+        t0 = time.perf_counter()
+        if kind == "softmax":
+            oracle.softmax_rows(inp)
+        else:
+            oracle.layernorm_rows(*inp, 1e-5)
+        return time.perf_counter() - t0
+
+    r = 1
+    dt = timed(r)
+    while dt * 2 < target_seconds and r < 4096:
+        r *= 2
+        dt = timed(r)
+    desc = f"{r} rows of length {N}, fp64, 1 thread (plain loops)"
+    return 4.0 * r * N / dt / 1e9, dt, r, desc
+
+
+def run_gb300_rows(args, kind):
+    import torch
+
+    import exact_long_sequence_gb300 as ela
+    from exact_long_sequence_gb300 import _build, workloads
+
+    name = args.workload or ("softmax_r16384_n16384" if kind == "softmax" else "layernorm_r65536_n8192")
+    if name not in workloads.ROW_WORKLOADS or workloads.ROW_WORKLOADS[name][0] != kind:
+        raise SystemExit(f"unknown {kind} workload {name}; choose from "
+                         f"{[k for k, v in workloads.ROW_WORKLOADS.items() if v[0] == kind]}")
+    _, R, N = workloads.ROW_WORKLOADS[name]
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (sm_103a); no CPU fallback exists")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or not os.path.exists(ela.LIB_PATH):
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    ela.load_library()
+    stream = torch.cuda.current_stream(dev)
+    inp = workloads.row_inputs(kind, R, N, seed=1, device=dev)
+    out = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    ws_bytes = ela.load_library().attn_softmax_rows_workspace_bytes(R, N) if kind == "softmax" else 0
+    ws = torch.empty(max(ws_bytes, 8), dtype=torch.uint8, device=dev) if ws_bytes else None
+    passes = 1 if kind == "layernorm" or ws_bytes == 0 else 2  # reads of x per step
+
+    def step():
+        if kind == "softmax":
+            ela.softmax_rows(inp, out=out, workspace=ws, stream=stream)
+        else:
+            ela.layernorm_rows(*inp, eps=1e-5, out=out, stream=stream)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    slowest = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    alg_bytes = 4.0 * R * N + (4.0 * N if kind == "layernorm" else 0.0)  # one bf16 read and write per element
+    value = alg_bytes * args.steps * world / slowest / 1e9
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind = read_hbm_peak()
+    kernel_ms = statistics.mean(step_ms)
+    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    line = {
+        "metric": f"standalone streaming {kind} GB/s (one bf16 read and write per element) on 1 GB300",
+        "pass": kind, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": slowest * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "R": R, "N": N, "inputs": "seeded synthetic normal rows, bf16",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)",
+                   "parallelism": "replicas", "reads_of_x_per_step": passes},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json)", "traffic": None,
+                     "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kernel_ms},
+        "gpu_launches": args.steps * (1 if passes == 1 else 2), "clocks": clocks.summary(),
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+        "e2e": None,
+    }
+    if not args.skip_cpu and world == 1:
+        v_cpu, dt, r, desc = cpu_oracle_rows_sample(kind, N, min(args.cpu_seconds, 5.0))
+        line["cpu_baseline"] = {"value": v_cpu, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+                                "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_gb300_bwd(args, w):
     import torch
 
@@ -635,6 +766,8 @@ def main(argv=None):
     args = parse_args(argv)
     from exact_long_sequence_gb300 import workloads
 
+    if args.which in ("softmax", "layernorm"):
+        return run_gb300_rows(args, args.which)
     name = args.workload or workloads.HEADLINE
     if name not in workloads.WORKLOADS:
         raise SystemExit(f"unknown workload {name}; choose from {sorted(workloads.WORKLOADS)}")

@@ -46,6 +46,9 @@ EXPORTED_SYMBOLS = (
     "attn_bwd_workspace_bytes",
     "attn_fwd_fp8",
     "attn_fwd_fp8_workspace_bytes",
+    "attn_softmax_rows",
+    "attn_softmax_rows_workspace_bytes",
+    "attn_layernorm_rows",
 )
 
 
@@ -113,6 +116,13 @@ def load_library(path: str | None = None):
     lib.attn_fwd_fp8.restype = i
     lib.attn_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
     lib.attn_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
+    i64 = ctypes.c_int64
+    lib.attn_softmax_rows.argtypes = [vp, vp, i64, i, vp, ctypes.c_size_t, vp]
+    lib.attn_softmax_rows.restype = i
+    lib.attn_softmax_rows_workspace_bytes.argtypes = [i64, i]
+    lib.attn_softmax_rows_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_layernorm_rows.argtypes = [vp, vp, vp, vp, i64, i, f, vp]
+    lib.attn_layernorm_rows.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -227,6 +237,48 @@ def attn_fwd_fp8(q8, k8, v8, scales, causal: bool = False, scale: float | None =
                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st, "attn_fwd_fp8")
     return out, lse
+
+
+def softmax_rows(x, out=None, workspace=None, stream=None):
+    """Row softmax over the last axis of a contiguous bf16 CUDA tensor (last axis a multiple of 8)."""
+    import torch
+
+    lib = load_library()
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 CUDA tensor")
+    N = x.shape[-1]
+    R = x.numel() // N
+    if out is None:
+        out = torch.empty_like(x)
+    need = lib.attn_softmax_rows_workspace_bytes(R, N)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    with torch.cuda.device(x.device):
+        st = lib.attn_softmax_rows(x.data_ptr(), out.data_ptr(), R, N,
+                                   workspace.data_ptr() if workspace is not None else None,
+                                   workspace.numel() if workspace is not None else 0, _stream_handle(stream))
+    _check(st, "attn_softmax_rows")
+    return out
+
+
+def layernorm_rows(x, gamma, beta, eps: float = 1e-5, out=None, stream=None):
+    """Layer normalisation over the last axis (bf16 x, gamma, beta on CUDA; last axis a multiple of 8, <= 65536)."""
+    import torch
+
+    lib = load_library()
+    for t in (x, gamma, beta):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("x, gamma, beta must be contiguous bf16 CUDA tensors")
+    N = x.shape[-1]
+    if gamma.shape != (N,) or beta.shape != (N,):
+        raise ValueError("gamma and beta must have the row length")
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        st = lib.attn_layernorm_rows(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), out.data_ptr(),
+                                     x.numel() // N, N, float(eps), _stream_handle(stream))
+    _check(st, "attn_layernorm_rows")
+    return out
 
 
 def attn_fwd_noalloc(q, k, v, out, lse, causal: bool = False, scale: float | None = None, stream=None):

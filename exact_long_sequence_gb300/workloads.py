@@ -136,3 +136,25 @@ def workload_rows(w: Workload):
     if w.oracle_rows is None:
         return None
     return sample_rows(w.B * w.H, w.N, w.oracle_rows, w.seed)
+
+
+# Standalone streaming row operations: (R rows, N elements per row), bf16, seeded
+# normal inputs (softmax: N(0, 3^2); layer normalisation: N(3, 1) with gamma
+# ~ 1 + 0.2 N(0, 1) and beta ~ 0.3 N(0, 1)).  Sized well above L2 so that the
+# rate measured is the HBM rate.
+ROW_WORKLOADS = {
+    "softmax_r16384_n16384": ("softmax", 16384, 16384),      # attention-score-shaped rows, 512 MiB each way
+    "softmax_r64_n1048576": ("softmax", 64, 1 << 20),        # million-element rows: the segmented path
+    "layernorm_r65536_n8192": ("layernorm", 65536, 8192),    # 1 GiB each way
+}
+
+
+def row_inputs(kind: str, R: int, N: int, seed: int = 0, device="cpu"):
+    """Seeded inputs of a row workload: x, or (x, gamma, beta) for layer normalisation."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    if kind == "softmax":
+        return (torch.randn(R, N, generator=g, device=device) * 3).to(torch.bfloat16)
+    x = (torch.randn(R, N, generator=g, device=device) + 3).to(torch.bfloat16)
+    gamma = (1 + 0.2 * torch.randn(N, generator=g, device=device)).to(torch.bfloat16)
+    beta = (0.3 * torch.randn(N, generator=g, device=device)).to(torch.bfloat16)
+    return x, gamma, beta

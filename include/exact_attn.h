@@ -216,6 +216,46 @@ int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void* O, float*
 /* Device bytes attn_fwd_fp8 needs as workspace: B*H*d*ceil16(N); 0 for a non-positive size. */
 size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
 
+/*
+ * attn_softmax_rows - standalone streaming row softmax ("Softmax streaming",
+ * section 8 of "From Attention Graph to FlashAttention - A Memory-Centric
+ * Compilation Approach in AICF"):
+ *     Y[r, i] = exp(X[r, i] - max_j X[r, j]) / sum_j exp(X[r, j] - max_j X[r, j])
+ * with the row statistics gathered in one pass by the online-softmax
+ * recurrence and fp32 arithmetic.
+ *   X, Y      : bf16 [R, N] row-major device arrays, 16-byte aligned (may alias: in place is allowed)
+ *   R, N      : 1 <= R < 2^31; N >= 1 and a multiple of 8 (ATTN_ERR_UNSUPPORTED otherwise)
+ *   workspace : needed when N > 65536: attn_softmax_rows_workspace_bytes() bytes,
+ *               8-byte aligned, owned by the caller; may be NULL otherwise
+ * Rows of N <= 65536 are held by one CTA; rows of up to 4 * 65536 by a
+ * thread-block cluster of ceil(N / 65536) CTAs that exchange their partial
+ * statistics through distributed shared memory: both read X once and write Y
+ * once.  Longer rows (or a device that cannot hold the cluster) are handled in
+ * segments of 16384 with a second read of X, using the workspace for the
+ * per-segment statistics.  Asynchronous on `stream`.
+ */
+int attn_softmax_rows(const void* X, void* Y, int64_t R, int N, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/* Device bytes attn_softmax_rows needs as workspace (0 when N <= 65536). */
+size_t attn_softmax_rows_workspace_bytes(int64_t R, int N);
+
+/*
+ * attn_layernorm_rows - standalone streaming layer normalisation ("LayerNorm
+ * streaming", same section): per row,
+ *     mean = sum_j x_j / N,  var = sum_j (x_j - mean)^2 / N,
+ *     Y[r, i] = (X[r, i] - mean) / sqrt(var + eps) * gamma[i] + beta[i],
+ * the statistics gathered in one pass (running mean and sum of squared
+ * deviations, merged pairwise) in fp32.
+ *   X, Y        : bf16 [R, N] row-major device arrays, 16-byte aligned (in place is allowed)
+ *   gamma, beta : bf16 [N] device arrays, 16-byte aligned
+ *   R, N        : 1 <= R < 2^31; N a multiple of 8, at most 65536 (ATTN_ERR_UNSUPPORTED otherwise)
+ *   eps         : finite, >= 0
+ * Each row is read once and written once.  Asynchronous on `stream`.
+ */
+int attn_layernorm_rows(const void* X, const void* gamma, const void* beta, void* Y, int64_t R, int N, float eps,
+                        cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

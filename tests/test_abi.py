@@ -137,3 +137,30 @@ def test_package_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text and "attn_oracle" not in text, f
+
+
+def test_fp8_entry_validation(lib):
+    args = (0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1, 1, 128)
+    ws = (0x6000, 1 << 20, None)
+    assert lib.attn_fwd_fp8(*args, 64, 0, 0.125, 1.0, 1.0, 1.0, *ws) == ela.ATTN_ERR_UNSUPPORTED
+    for bad in ((0.0, 1.0, 1.0), (1.0, float("inf"), 1.0), (1.0, 1.0, -2.0)):
+        assert lib.attn_fwd_fp8(*args, 128, 0, 0.125, *bad, *ws) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_fp8(*args, 128, 0, 0.125, 1.0, 1.0, 1.0, None, 1 << 20, None) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_fp8(*args, 128, 0, 0.125, 1.0, 1.0, 1.0, 0x6000, 16, None) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_fp8_workspace_bytes(2, 3, 100, 128) == 2 * 3 * 128 * 112
+
+
+def test_row_ops_validation(lib):
+    assert lib.attn_softmax_rows(None, 0x2000, 4, 64, None, 0, None) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_softmax_rows(0x1000, 0x2000, 0, 64, None, 0, None) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_softmax_rows(0x1000, 0x2000, 4, 60, None, 0, None) == ela.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_softmax_rows(0x1008, 0x2000, 4, 64, None, 0, None) == ela.ATTN_ERR_MISALIGNED
+    # long rows need the segment workspace: R * ceil(N / 16384) (m, l) pairs of 8 bytes
+    assert lib.attn_softmax_rows_workspace_bytes(3, 1 << 16) == 0
+    assert lib.attn_softmax_rows_workspace_bytes(3, (1 << 16) + 8) == 3 * 5 * 8
+    assert lib.attn_softmax_rows(0x1000, 0x2000, 3, (1 << 16) + 8, None, 0, None) == ela.ATTN_ERR_INVALID_ARG
+    g, b = 0x3000, 0x4000
+    assert lib.attn_layernorm_rows(0x1000, g, b, 0x2000, 4, (1 << 16) + 8, 1e-5, None) == ela.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_layernorm_rows(0x1000, g, b, 0x2000, 4, 64, -1.0, None) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_layernorm_rows(0x1000, None, b, 0x2000, 4, 64, 1e-5, None) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_layernorm_rows(0x1000, 0x3004, b, 0x2000, 4, 64, 1e-5, None) == ela.ATTN_ERR_MISALIGNED
