@@ -10,6 +10,7 @@
 
 #include "../../include/exact_attn.h"
 #include "api_common.h"
+#include "attn_fwd_fp8_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "plan.h"
 
@@ -59,8 +60,8 @@ __global__ void __launch_bounds__(256) transpose_v_e4m3(const uint8_t* V, uint8_
 template <bool CAUSAL>
 int launch_fp8(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, const CUtensorMap& tk,
                const CUtensorMap& tvt, const FwdParams& p, cudaStream_t stream) {
-    auto kernel = attn_fwd_kernel<kFp8D, CAUSAL, true>;
-    constexpr int smem = smem_bytes_for(kFp8D, 1);
+    auto kernel = attn_fwd_fp8_kernel<CAUSAL>;
+    constexpr int smem = Fp8Layout::kSmem;
     bool& configured = dev.fp8_smem_configured[CAUSAL];
     cudaError_t e;
     if (!configured) {

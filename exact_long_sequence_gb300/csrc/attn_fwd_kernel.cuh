@@ -26,13 +26,6 @@
 // after O_t += P_t V has been issued; tcgen05.mma operations of one thread run
 // in issue order on the SM's tensor core.
 //
-// FP8 variant (template flag FP8): Q, K arrive as E4M3 codes [BH, N, d] and V
-// as E4M3 codes transposed to [BH, d, N] (so that both products read K-major
-// operands); S = Q K^T and O += P V run as tcgen05 kind::f8f6f4 with K = 32 per
-// instruction, P is packed to E4M3 (four per TMEM column, over the first 32
-// columns of S_t), and the per-tensor scales enter through scale_log2 (Q and
-// K) and out_scale (V).  Everything else is the bf16 kernel.
-//
 // Online softmax (the "streaming reformulation" of the IO-Aware Algorithms
 // page): per row, a reference maximum m (log2 units, scale folded in) and a
 // running sum l.  A tile whose row maximum exceeds m by more than
@@ -65,8 +58,8 @@ struct FwdParams {
     int num_pairs;         // ceil(num_q_tiles / 2): units per (batch, head)
     int num_units;         // BH * num_pairs
     int heads_per_group;   // causal schedule only
-    float scale_log2;      // scale * log2(e) (times the Q and K scales for FP8)
-    float out_scale;       // FP8: the V scale, applied with 1 / l; unused for bf16
+    float scale_log2;      // scale * log2(e) (times the Q and K scales for the FP8 kernel)
+    float out_scale;       // FP8 kernel: the V scale, applied with 1 / l; unused here
 };
 
 struct UnitInfo {
@@ -114,11 +107,10 @@ struct RingPos {
     }
 };
 
-template <int D, bool FP8 = false>
+template <int D>
 struct SmemLayout {
-    static constexpr int kEsize = FP8 ? 1 : 2;
-    static constexpr int kTile = tile_bytes(D, kEsize);
-    static constexpr int kStages = kv_stages_for(D, kEsize);
+    static constexpr int kTile = tile_bytes(D);
+    static constexpr int kStages = kv_stages_for(D);
     static constexpr int kQOff = 0;
     static constexpr int kRingOff = kQTiles * kTile;
     static constexpr int kBarOff = kRingOff + kStages * kTile;
@@ -137,17 +129,14 @@ struct SmemLayout {
     static constexpr int kFlagsOff = kBarOff + kNumBars * 8;  // tmem base slot, abort flag
     static constexpr int kBytes = kFlagsOff + 16;
     static_assert(kNumBars == 2 * kStages + kFixedBarriers, "barrier count differs from the plan");
-    static_assert(kBytes + kSmemAlign <= smem_bytes_for(D, kEsize), "shared memory layout exceeds the plan");
-    static_assert(!FP8 || D == 128, "the E4M3 tiles are one 128-byte swizzle row wide");
+    static_assert(kBytes + kSmemAlign <= smem_bytes_for(D), "shared memory layout exceeds the plan");
 };
 
-template <int D, bool CAUSAL, bool FP8 = false>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
-    using L = SmemLayout<D, FP8>;
-    // 128-byte swizzle rows per tile row: 64 bf16 or 128 E4M3 columns each
-    constexpr int kRowBlocks = FP8 ? 1 : D / 64;
+    using L = SmemLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
@@ -206,7 +195,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTile);
                 const uint32_t dst = s_base + L::kQOff + t * L::kTile;
 #pragma unroll
-                for (int b = 0; b < kRowBlocks; ++b)
+                for (int b = 0; b < D / 64; ++b)
                     tma_load_3d(dst + b * (kBr * 128), &tmap_q, bar(L::kQFull + t), b * 64, (ui.q0 + t) * kBr, ui.bh);
                 q_issued |= 1u << t;
             }
@@ -219,17 +208,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     mbar_arrive_expect_tx(bar(L::kKvFull + pos.stage), L::kTile);
                     const uint32_t dst = s_base + L::kRingOff + pos.stage * L::kTile;
                     const CUtensorMap* tm = kv == 0 ? &tmap_k : &tmap_v;
-                    if constexpr (FP8) {
-                        if (kv == 0)  // K_j: [128 keys][d] codes
-                            tma_load_3d(dst, tm, bar(L::kKvFull + pos.stage), 0, j * kBc, ui.bh);
-                        else          // V_j^T: [d][128 keys] codes
-                            tma_load_3d(dst, tm, bar(L::kKvFull + pos.stage), j * kBc, 0, ui.bh);
-                    } else {
 #pragma unroll
-                        for (int b = 0; b < D / 64; ++b)
-                            tma_load_3d(dst + b * (kBc * 128), tm, bar(L::kKvFull + pos.stage), b * 64, j * kBc,
-                                        ui.bh);
-                    }
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(dst + b * (kBc * 128), tm, bar(L::kKvFull + pos.stage), b * 64, j * kBc, ui.bh);
                     pos = pos.next(L::kStages);
                     ++issued;
                 }
@@ -254,14 +235,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         // The whole warp runs the loop and waits; one elected lane issues the
         // MMAs and commits (a converged warp issues tcgen05.mma faster than a
         // lone divergent lane).
-        constexpr uint32_t idesc_s = FP8 ? make_idesc_e4m3_f32(kBr, kBc) : make_idesc_bf16_f32(kBr, kBc, false, false);
-        constexpr uint32_t idesc_o = FP8 ? make_idesc_e4m3_f32(kBr, D) : make_idesc_bf16_f32(kBr, D, false, true);
+        constexpr uint32_t idesc_s = make_idesc_bf16_f32(kBr, kBc, false, false);
+        constexpr uint32_t idesc_o = make_idesc_bf16_f32(kBr, D, false, true);
         // The descriptor's start-address field holds (address >> 4), so a move
-        // inside shared memory is an add on the descriptor.  V_j is MN-major
-        // for bf16 and K-major (stored transposed) for FP8.
+        // inside shared memory is an add on the descriptor.
         const uint64_t dq0 = make_smem_desc_sw128(s_base + L::kQOff, 16, 1024);
         const uint64_t dk0 = make_smem_desc_sw128(s_base + L::kRingOff, 16, 1024);
-        const uint64_t dv0 = make_smem_desc_sw128(s_base + L::kRingOff, FP8 ? 16 : kBc * 128, 1024);
+        const uint64_t dv0 = make_smem_desc_sw128(s_base + L::kRingOff, kBc * 128, 1024);
         RingPos kpos{0u, 0u};  // ring position of the next unit's K_0
         uint32_t ul = 0;
         uint32_t p_phase[2] = {0u, 0u};
@@ -270,38 +250,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         auto gemm_s = [&](int t, uint32_t slot) {
             const uint64_t a = dq0 + static_cast<uint64_t>((t * L::kTile) >> 4);
             const uint64_t b = dk0 + static_cast<uint64_t>((slot * L::kTile) >> 4);
-            if constexpr (FP8) {
-                // K = 32 codes (32 bytes) per instruction along the 128-byte row
 #pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
-                    mma_ss_f8(tmem + t * kBc, a + off, b + off, idesc_s, kk > 0 ? 1u : 0u);
-                }
-            } else {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBr * 128) + (kk & 3) * 32) >> 4);
-                    mma_ss(tmem + t * kBc, a + off, b + off, idesc_s, kk > 0 ? 1u : 0u);
-                }
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBr * 128) + (kk & 3) * 32) >> 4);
+                mma_ss(tmem + t * kBc, a + off, b + off, idesc_s, kk > 0 ? 1u : 0u);
             }
         };
         // O_t (+)= P_t V over keys [64 half, 64 half + 64) with V in ring stage
         // `slot`; P_t is read from TMEM.
         auto gemm_o = [&](int t, uint32_t slot, int half, bool accumulate) {
             const uint64_t b = dv0 + static_cast<uint64_t>((slot * L::kTile) >> 4);
-            if constexpr (FP8) {
-                // 32 keys per instruction: 8 TMEM columns of P (four codes each),
-                // 32 bytes along V_j^T's 128-byte rows
 #pragma unroll
-                for (int kk = half * 2; kk < half * 2 + 2; ++kk)
-                    mma_ts_f8(tmem + 2 * kBc + t * D, tmem + t * kBc + kk * 8,
-                              b + static_cast<uint64_t>((kk * 32) >> 4), idesc_o, (accumulate || kk > 0) ? 1u : 0u);
-            } else {
-#pragma unroll
-                for (int kk = half * 4; kk < half * 4 + 4; ++kk)
-                    mma_ts(tmem + 2 * kBc + t * D, tmem + t * kBc + kk * 8,
-                           b + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_o, (accumulate || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = half * 4; kk < half * 4 + 4; ++kk)
+                mma_ts(tmem + 2 * kBc + t * D, tmem + t * kBc + kk * 8,
+                       b + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_o, (accumulate || kk > 0) ? 1u : 0u);
         };
         for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
             const UnitInfo ui = decode_unit<CAUSAL>(u, p);
@@ -447,10 +409,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
                 l *= alpha;
                 // P = 2^(s*scale*log2e - m), packed as bf16 pairs over the first
-                // 64 columns of S_t (FP8: E4M3 quadruples over the first 32),
-                // stored 32 scores at a time.
+                // 64 columns of S_t, stored 16 columns (32 scores) at a time.
                 float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-                auto exp_chunk = [&](const float* sc, uint32_t chunk) {
+                auto exp_chunk = [&](const float* sc, uint32_t col) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int c = 0; c < 16; c += 2) {
@@ -462,22 +423,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         acc1 += b0;
                         acc2 += a1;
                         acc3 += b1;
-                        if constexpr (FP8) {
-                            pk[c / 2] = pack_e4m3x4(a0, b0, a1, b1);
-                        } else {
-                            pk[c] = pack_bf16x2(a0, b0);
-                            pk[c + 1] = pack_bf16x2(a1, b1);
-                        }
+                        pk[c] = pack_bf16x2(a0, b0);
+                        pk[c + 1] = pack_bf16x2(a1, b1);
                     }
-                    if constexpr (FP8) {
-                        const uint32_t(&pk8)[8] = *reinterpret_cast<const uint32_t(*)[8]>(pk);
-                        tmem_st8(t_s + chunk * 8, pk8);
-                    } else {
-                        tmem_st16(t_s + chunk * 16, pk);
-                    }
+                    tmem_st16(t_s + col, pk);
                 };
                 exp_chunk(s0, 0);
-                exp_chunk(s1, 1);
+                exp_chunk(s1, 16);
                 // Rescale the O accumulator when this row's reference max moved,
                 // before the first half of P_t is released to O_t += P_t V.
                 // O_t's previous P V has completed: it was issued before this
@@ -496,8 +448,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 tmem_wait_st();
                 tc_fence_before_sync();
                 mbar_arrive(bar(L::kPHalf + t));
-                exp_chunk(s2, 2);
-                exp_chunk(s3, 3);
+                exp_chunk(s2, 32);
+                exp_chunk(s3, 48);
                 l += (acc0 + acc1) + (acc2 + acc3);
                 tmem_wait_st();
                 tc_fence_before_sync();
@@ -509,8 +461,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             __syncwarp();
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after_sync();
-            float inv_l = 1.f / l;
-            if constexpr (FP8) inv_l *= p.out_scale;
+            const float inv_l = 1.f / l;
             const bool row_ok = qrow < p.N;
             const size_t grow_idx = static_cast<size_t>(ui.bh) * p.N + (row_ok ? qrow : 0);
             uint4* orow = reinterpret_cast<uint4*>(p.O + grow_idx * D);
