@@ -72,3 +72,25 @@ def test_backward_deterministic_dk_dv():
     torch.cuda.synchronize()
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])  # dK, dV have no atomics
     assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2 * a[0].float().abs().max().item()
+
+
+def test_backward_outputs_and_workspace_stay_inside_their_buffers():
+    """Guard canaries after dQ, dK, dV and after the workspace the call asked for stay untouched."""
+    B, H, N, d = 1, 2, 300, 128
+    q, k, v = (t.cuda() for t in workloads.make_inputs(B, H, N, d, seed=9))
+    do = workloads.make_inputs(B, H, N, d, seed=10)[0].cuda()
+    o, lse = ela.attn_fwd(q, k, v, causal=True)
+    lib = ela.load_library()
+    n = B * H * N * d
+    bufs = [torch.full((n + 4096,), 7.0, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    need = lib.attn_bwd_workspace_bytes(B, H, N, d)
+    ws = torch.full((need + 4096,), 0x5A, dtype=torch.uint8, device="cuda")
+    st = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                      bufs[0].data_ptr(), bufs[1].data_ptr(), bufs[2].data_ptr(), B, H, N, d, 1,
+                      ela.default_scale(d), ws.data_ptr(), need, None)
+    assert st == ela.ATTN_OK
+    torch.cuda.synchronize()
+    assert ela.last_device_error() == ela.ATTN_OK
+    for b in bufs:
+        assert (b[n:] == 7.0).all() and torch.isfinite(b[:n].float()).all()
+    assert (ws[need:] == 0x5A).all()

@@ -105,3 +105,19 @@ def test_fp8_rejects_bad_arguments():
     for bad in ((0.0, 1.0, 1.0), (1.0, float("nan"), 1.0), (1.0, 1.0, -1.0)):
         with pytest.raises(ela.AttnError):
             ela.attn_fwd_fp8(q8, q8, q8, bad)
+
+
+def test_fp8_outputs_and_workspace_stay_inside_their_buffers():
+    B, H, N = 1, 2, 300
+    q8, k8, v8, sc = workloads.make_inputs_fp8(B, H, N, D, seed=11)
+    n = B * H * N * D
+    o_buf = torch.full((n + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((B * H * N + 1024,), 7.0, dtype=torch.float32, device="cuda")
+    need = ela.load_library().attn_fwd_fp8_workspace_bytes(B, H, N, D)
+    ws = torch.full((need + 4096,), 0x5A, dtype=torch.uint8, device="cuda")
+    o = o_buf[:n].view(B, H, N, D)
+    lse = l_buf[: B * H * N].view(B, H, N)
+    ela.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), sc, causal=True, out=o, lse=lse, workspace=ws[:need])
+    torch.cuda.synchronize()
+    assert ela.last_device_error() == ela.ATTN_OK
+    assert (o_buf[n:] == 7.0).all() and (l_buf[B * H * N:] == 7.0).all() and (ws[need:] == 0x5A).all()

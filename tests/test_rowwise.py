@@ -92,3 +92,21 @@ def test_row_ops_reject_bad_shapes():
     g = torch.ones(65544, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ela.AttnError):
         ela.layernorm_rows(x, g, g)  # longer than one CTA holds
+
+
+@pytest.mark.parametrize("N", [1000, 65544, (1 << 20) + 8])
+def test_row_outputs_and_workspace_stay_inside_their_buffers(N):
+    N = (N + 7) // 8 * 8
+    R = 3
+    x = rows(R, N, seed=N).cuda()
+    y_buf = torch.full((R * N + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    need = ela.load_library().attn_softmax_rows_workspace_bytes(R, N)
+    ws = torch.full((need + 4096,), 0x5A, dtype=torch.uint8, device="cuda")
+    ela.softmax_rows(x, out=y_buf[: R * N].view(R, N), workspace=ws[:need] if need else None)
+    torch.cuda.synchronize()
+    assert (y_buf[R * N:] == 7.0).all() and (ws[need:] == 0x5A).all()
+    g = torch.ones(N, dtype=torch.bfloat16, device="cuda")
+    if N <= 65536:
+        ela.layernorm_rows(x, g, g, out=y_buf[: R * N].view(R, N))
+        torch.cuda.synchronize()
+        assert (y_buf[R * N:] == 7.0).all()
