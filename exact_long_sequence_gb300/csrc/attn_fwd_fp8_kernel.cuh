@@ -380,14 +380,15 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                     uint32_t pk[8];
 #pragma unroll
                     for (int c = 0; c < 16; c += 2) {
-                        const float a0 = ex2_approx(fmaf(sc[2 * c], sl2, -m_use));
-                        const float b0 = ex2_approx(fmaf(sc[2 * c + 1], sl2, -m_use));
-                        const float a1 = ex2_approx(fmaf(sc[2 * c + 2], sl2, -m_use));
-                        const float b1 = ex2_approx(fmaf(sc[2 * c + 3], sl2, -m_use));
-                        acc0 += a0;
-                        acc1 += b0;
-                        acc2 += a1;
-                        acc3 += b1;
+                        float x0, x1, x2, x3;  // exponents, two per packed instruction
+                        ffma2(x0, x1, sc[2 * c], sc[2 * c + 1], sl2, -m_use);
+                        ffma2(x2, x3, sc[2 * c + 2], sc[2 * c + 3], sl2, -m_use);
+                        const float a0 = ex2_approx(x0);
+                        const float b0 = ex2_approx(x1);
+                        const float a1 = ex2_approx(x2);
+                        const float b1 = ex2_approx(x3);
+                        fadd2(acc0, acc1, a0, b0);
+                        fadd2(acc2, acc3, a1, b1);
                         pk[c / 2] = pack_e4m3x4(a0, b0, a1, b1);
                     }
 #pragma unroll

@@ -323,6 +323,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// Packed fp32 pairs (one instruction for two lanes of arithmetic):
+//   (x0, x1) = (a0 * b + c, a1 * b + c),  each correctly rounded like fmaf;
+//   (s0, s1) += (a0, a1),                  each correctly rounded like a float add.
+__device__ __forceinline__ void ffma2(float& x0, float& x1, float a0, float a1, float b, float c) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 pa, pb, pc;\n\tmov.b64 pa, {%1, %2};\n\tmov.b64 pb, {%3, %3};\n\t"
+        "mov.b64 pc, {%4, %4};\n\tfma.rn.f32x2 %0, pa, pb, pc;\n\t}"
+        : "=l"(r)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(r));
+}
+__device__ __forceinline__ void fadd2(float& s0, float& s1, float a0, float a1) {
+    uint64_t r;
+    asm("{\n\t.reg .b64 pa, pb;\n\tmov.b64 pa, {%1, %2};\n\tmov.b64 pb, {%3, %4};\n\tadd.rn.f32x2 %0, pa, pb;\n\t}"
+        : "=l"(r)
+        : "f"(s0), "f"(s1), "f"(a0), "f"(a1));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(r));
+}
+
 // Four floats -> four E4M3 bytes (round to nearest, saturating), x0 in the lowest byte.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
     uint16_t lo, hi;
