@@ -80,9 +80,9 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
         const auto* o = static_cast<const __nv_bfloat16*>(O);
         const auto* g = static_cast<const __nv_bfloat16*>(dO);
         if (d == 64)
-            attn_bwd_prep_kernel<64><<<blocks, 256, 0, stream>>>(o, g, LSE, dvec, lse2, dqacc, N, Np, padded);
+            attn_bwd_prep_kernel<64><<<blocks, 256, 0, stream>>>(o, g, LSE, dvec, lse2, dqacc, N, Np, padded, scale);
         else
-            attn_bwd_prep_kernel<128><<<blocks, 256, 0, stream>>>(o, g, LSE, dvec, lse2, dqacc, N, Np, padded);
+            attn_bwd_prep_kernel<128><<<blocks, 256, 0, stream>>>(o, g, LSE, dvec, lse2, dqacc, N, Np, padded, scale);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e);
     }

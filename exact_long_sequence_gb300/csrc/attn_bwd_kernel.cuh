@@ -52,8 +52,8 @@ constexpr int bwd_stages(int d) { return d == 128 ? 3 : 4; }
 
 struct BwdParams {
     float* dQacc;          // [BH, N, d] fp32, zeroed; receives scale * dS K
-    const float* lse2;     // [BH, Np] LSE * log2(e) of the forward; +inf on the padding rows
-    const float* Dvec;     // [BH, Np] D_i = sum_c dO_ic O_ic; 0 on the padding rows
+    const float* lse2;     // [BH, Np] -LSE * log2(e) of the forward; -inf on the padding rows
+    const float* Dvec;     // [BH, Np] -scale * D_i, D_i = sum_c dO_ic O_ic; 0 on the padding rows
     __nv_bfloat16* dK;     // [BH, N, d]
     __nv_bfloat16* dV;     // [BH, N, d]
     uint32_t* error_word;
@@ -288,6 +288,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         __syncwarp();
         mbar_wait_drain(bar(L::kDrain), 0, 1000000000ull);
     } else if ((warp >= 4 && warp < 8) || warp >= 12) {
+        // (x0, x1) = (a0 * b + c0, a1 * b + c1) and (x0, x1) *= (m0, m1) on packed fp32 pairs
+        auto ffma2c = [](float& x0, float& x1, float a0, float a1, float b, float c0, float c1) {
+            uint64_t rr;
+            asm("{\n\t.reg .b64 pa, pb, pc;\n\tmov.b64 pa, {%1, %2};\n\tmov.b64 pb, {%3, %3};\n\t"
+                "mov.b64 pc, {%4, %5};\n\tfma.rn.f32x2 %0, pa, pb, pc;\n\t}"
+                : "=l"(rr) : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(rr));
+        };
+        auto fmul2 = [](float& x0, float& x1, float m0, float m1) {
+            uint64_t rr;
+            asm("{\n\t.reg .b64 pa, pb;\n\tmov.b64 pa, {%1, %2};\n\tmov.b64 pb, {%3, %4};\n\tmul.rn.f32x2 %0, pa, pb;\n\t}"
+                : "=l"(rr) : "f"(x0), "f"(x1), "f"(m0), "f"(m1));
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(rr));
+        };
         // ------------------------------------------------------------ P and dS
         // Thread r = key row r of the tile (TMEM lane r).  Warps 4-7 take the
         // block's queries 0-31, warps 12-15 queries 32-63.  Every tcgen05.ld/st
@@ -314,6 +328,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (!ok) break;
             tc_fence_after_sync();
             // P^T = exp2(S^T * scale * log2e - LSE * log2e), masked -> bf16 over S^T's first 32 columns
+            // (the statistics hold -LSE * log2e and -scale * D)
             {
                 uint32_t sv[32];
                 tmem_ld32(t_s + c0, sv);
@@ -325,14 +340,27 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
                 tmem_wait_ld(sv);
                 uint32_t pk[16];
+                // masking is needed only in tiles that hold a padding key or cross the diagonal
+                const bool need_mask = __any_sync(0xffffffffu, key >= p.N || (CAUSAL && key > q0 + c0));
+                if (need_mask) {
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const int qa = q0 + c0 + c;
-                    float a = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -l[c]));
-                    float bb = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), sl2, -l[c + 1]));
-                    if (key >= p.N || (CAUSAL && key > qa)) a = 0.f;
-                    if (key >= p.N || (CAUSAL && key > qa + 1)) bb = 0.f;
-                    pk[c / 2] = pack_bf16x2(a, bb);
+                    for (int c = 0; c < 32; c += 2) {
+                        const int qa = q0 + c0 + c;
+                        float a, bb;
+                        ffma2c(a, bb, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, l[c], l[c + 1]);
+                        a = ex2_approx(a);
+                        bb = ex2_approx(bb);
+                        if (key >= p.N || (CAUSAL && key > qa)) a = 0.f;
+                        if (key >= p.N || (CAUSAL && key > qa + 1)) bb = 0.f;
+                        pk[c / 2] = pack_bf16x2(a, bb);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        float a, bb;
+                        ffma2c(a, bb, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, l[c], l[c + 1]);
+                        pk[c / 2] = pack_bf16x2(ex2_approx(a), ex2_approx(bb));
+                    }
                 }
                 tmem_st16(t_s + c0, pk);  // over this warpgroup's own S^T columns
             }
@@ -363,8 +391,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
                     const float pa = __uint_as_float(pv[c / 2] << 16), pb = __uint_as_float(pv[c / 2] & 0xffff0000u);
-                    const float a = p.scale * pa * (__uint_as_float(dv[c]) - dd[c]);
-                    const float bb = p.scale * pb * (__uint_as_float(dv[c + 1]) - dd[c + 1]);
+                    float a, bb;  // scale * dP - scale * D, then times P
+                    ffma2c(a, bb, __uint_as_float(dv[c]), __uint_as_float(dv[c + 1]), p.scale, dd[c], dd[c + 1]);
+                    fmul2(a, bb, pa, pb);
                     pk[c / 2] = pack_bf16x2(a, bb);
                 }
                 tmem_st16(t_dp + c0, pk);  // over this warpgroup's own dP^T columns
@@ -502,12 +531,14 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 
 // Per-row statistics of the backward, on rows padded to whole key tiles
 // (Np = ceil(N / 128) * 128 per (batch, head)):
-//     D_i = sum_c dO_ic O_ic (fp32), lse2_i = LSE_i * log2(e);
-// padding rows get D = 0 and lse2 = +inf (so that exp2(. - lse2) = 0 there).
+//     D_i = sum_c dO_ic O_ic (fp32), stored as Dvec_i = -scale * D_i, and
+//     lse2_i = -LSE_i * log2(e),
+// negated so that the gradient kernel adds them inside packed FMAs; padding rows
+// get Dvec = 0 and lse2 = -inf (so that exp2(. + lse2) = 0 there).
 // Also zeroes the dQ accumulator.  D/8 threads per padded row, 8 elements each.
 template <int D>
 __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* O, const __nv_bfloat16* dO, const float* LSE,
-                                     float* Dvec, float* lse2, float* dQacc, int N, int Np, size_t padded_rows) {
+                                     float* Dvec, float* lse2, float* dQacc, int N, int Np, size_t padded_rows, float scale) {
     constexpr int kTpr = D / 8;
     const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const size_t prow = tid / kTpr;
@@ -532,8 +563,8 @@ __global__ void attn_bwd_prep_kernel(const __nv_bfloat16* O, const __nv_bfloat16
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (prow < padded_rows && part == 0) {
-        Dvec[prow] = acc;
-        lse2[prow] = live ? LSE[row] * 1.4426950408889634f : INFINITY;
+        Dvec[prow] = -scale * acc;
+        lse2[prow] = live ? -(LSE[row] * 1.4426950408889634f) : -INFINITY;
     }
 }
 
