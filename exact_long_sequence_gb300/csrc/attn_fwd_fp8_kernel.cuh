@@ -315,15 +315,18 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                                                  mbar_wait(bar(L::kPFree + 2 * t + pb), ((s_cnt >> 1) & 1u) ^ 1u, ctx));
                 if (!ok) break;
                 tc_fence_after_sync();
-                // Load S_t in two halves: the second half is in flight while the
-                // first is masked and reduced; then S_t's columns are released.
+                // Load S_t (all four loads in flight, one wait) and release its columns.
                 uint32_t r0[32], r1[32], r2[32], r3[32];
                 tmem_ld32(t_s + 0, r0);
                 tmem_ld32(t_s + 32, r1);
-                tmem_wait_ld(r0);
-                tmem_wait_ld(r1);
                 tmem_ld32(t_s + 64, r2);
                 tmem_ld32(t_s + 96, r3);
+                tmem_wait_ld(r0);
+                tmem_wait_ld(r1);
+                tmem_wait_ld(r2);
+                tmem_wait_ld(r3);
+                tc_fence_before_sync();
+                mbar_arrive(bar(L::kSCons + t));  // S_t's columns may take the next scores
                 float* s0 = reinterpret_cast<float*>(r0);
                 float* s1 = reinterpret_cast<float*>(r1);
                 float* s2 = reinterpret_cast<float*>(r2);
@@ -345,10 +348,6 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                     mx1 = fmax3(mx1, s1[c], s1[c + 1]);
                 }
                 mx0 = fmax3(mx0, s0[31], fmaxf(mx1, s1[31]));
-                tmem_wait_ld(r2);
-                tmem_wait_ld(r3);
-                tc_fence_before_sync();
-                mbar_arrive(bar(L::kSCons + t));  // S_t's columns may take the next scores
                 if (need_mask) {
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
