@@ -36,6 +36,8 @@ EXPORTED_SYMBOLS = (
     "attn_fwd",
     "attn_fwd_host",
     "attn_fwd_host_workspace_bytes",
+    "attn_fwd_split",
+    "attn_fwd_split_workspace_bytes",
     "attn_plan",
     "attn_last_device_error",
     "attn_last_cuda_error",
@@ -96,6 +98,10 @@ def load_library(path: str | None = None):
     lib.attn_fwd_host.restype = i
     lib.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i]
     lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_fwd_split.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
+    lib.attn_fwd_split.restype = i
+    lib.attn_fwd_split_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.attn_fwd_split_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(AttnPlan)]
     lib.attn_plan.restype = i
     lib.attn_last_device_error.argtypes = [vp]
@@ -147,12 +153,22 @@ def _stream_handle(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+def split_workspace_bytes(B: int, H: int, N: int, d: int, causal: bool) -> int:
+    """Device bytes attn_fwd_split needs for this shape on the current device (0: it would not split)."""
+    return int(load_library().attn_fwd_split_workspace_bytes(B, H, N, d, int(bool(causal))))
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
+             split: bool = True, workspace=None):
     """O, LSE = attention(q, k, v) on the GPU through the C ABI.
 
-    q, k, v : bf16 CUDA tensors [B, H, N, d], contiguous, d in {64, 128}
-    out     : optional bf16 [B, H, N, d] output buffer; lse: optional fp32 [B, H, N]
-    stream  : torch.cuda.Stream (default: the current stream); the call is asynchronous.
+    q, k, v   : bf16 CUDA tensors [B, H, N, d], contiguous, d in {64, 128}
+    out       : optional bf16 [B, H, N, d] output buffer; lse: optional fp32 [B, H, N]
+    stream    : torch.cuda.Stream (default: the current stream); the call is asynchronous.
+    split     : allow the K/V split of attn_fwd_split for problems with fewer work units than
+                SMs (False: always the single-kernel attn_fwd)
+    workspace : optional uint8 CUDA tensor of at least split_workspace_bytes() bytes for the
+                split (allocated here when needed and not given)
     """
     import torch
 
@@ -174,9 +190,22 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
     with torch.cuda.device(q.device):
-        st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                          B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
-    _check(st, "attn_fwd")
+        need = int(lib.attn_fwd_split_workspace_bytes(B, H, N, d, int(bool(causal)))) if split else 0
+        if need == 0:
+            st = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                              B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+            _check(st, "attn_fwd")
+            return out, lse
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            if stream is not None:
+                workspace.record_stream(stream)
+        if workspace.dtype != torch.uint8 or not workspace.is_cuda or workspace.numel() < need:
+            raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {need} bytes")
+        st = lib.attn_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                B, H, N, d, int(bool(causal)), float(scale), workspace.data_ptr(),
+                                workspace.numel(), _stream_handle(stream))
+    _check(st, "attn_fwd_split")
     return out, lse
 
 

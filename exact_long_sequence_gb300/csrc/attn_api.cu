@@ -30,10 +30,149 @@ int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, con
         if (e != cudaSuccess) return cuda_fail(e);
         configured = true;
     }
-    kernel<<<plan.grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
+    const int grid = p.kv_split > 1 ? (p.num_items < dev.num_sms ? p.num_items : dev.num_sms) : plan.grid;
+    kernel<<<grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
+    if (p.kv_split > 1) {
+        // programmatic dependent launch: the combine kernel's CTAs may start as the
+        // attention kernel's retire, and wait in-kernel for its completion
+        const size_t rows = static_cast<size_t>(p.BH) * p.N;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, attn_fwd_combine_kernel<D, CAUSAL>, p)) != cudaSuccess) return cuda_fail(e);
+    }
     return ATTN_OK;
+}
+
+// Units the split policy considers (a launch with more units than SMs is not split).
+constexpr int kMaxUnitsForSplit = 1024;
+
+struct KvSplit {
+    int segs;   // segments per split unit (1: no split)
+    int units;  // how many units, first in schedule order, are split
+};
+
+// Cost of the combine kernel, in K/V steps of one unit (measured: about 4 us
+// against about 1.2 us per K/V step of a query-tile pair).
+constexpr int kCombineSteps = 4;
+
+// The K/V split for a launch on num_sms SMs.  Only SMs that the units leave
+// idle take extra segments, so the launch stays one wave; the estimated time is
+// the longest work item in K/V steps (one step = one K/V tile for the pair),
+// plus the combine kernel.  A unit takes s segments only when s (s - 1) < n0
+// (see decode_item).  The host walks the units in the kernel's schedule order
+// (decode_unit); a split is kept only when it shortens the estimate.
+KvSplit choose_kv_split(const attn_plan_t& plan, int num_sms, int BH, int N, int causal) {
+    KvSplit best{1, 0};
+    const int units = plan.num_units;
+    if (units >= num_sms || units < 1) return best;
+    const int nq = (N + kBr - 1) / kBr, nkv = (N + kBc - 1) / kBc, pairs = (nq + 1) / 2;
+    const int G = plan.heads_per_group > 0 ? plan.heads_per_group : 1;
+    int n0[kMaxUnitsForSplit], n1[kMaxUnitsForSplit];
+    if (units > kMaxUnitsForSplit) return best;
+    int longest = 0;
+    for (int u = 0; u < units; ++u) {
+        int pair;
+        if (!causal) {
+            pair = u % pairs;
+        } else {
+            const int g = u / (G * pairs), r = u - g * G * pairs;
+            const int heads_here = (BH - g * G) < G ? (BH - g * G) : G;
+            pair = pairs - 1 - r / heads_here;
+        }
+        const int q0 = 2 * pair;
+        n0[u] = causal ? (q0 + 1 < nkv ? q0 + 1 : nkv) : nkv;
+        n1[u] = causal ? (q0 + 2 < nkv ? q0 + 2 : nkv) : nkv;
+        if (n1[u] > longest) longest = n1[u];
+    }
+    int best_cost = longest;
+    for (int s = 2; s <= kMaxKvSplit; ++s) {
+        int U = (num_sms - units) / (s - 1);
+        if (U > units) U = units;
+        int k = 0;
+        while (k < U && s * (s - 1) < n0[k]) ++k;  // a prefix of units that can take s segments
+        U = k;
+        if (U == 0) continue;
+        int cost = 0;
+        for (int u = 0; u < units; ++u) {
+            const int steps = u < U ? (n1[u] + s - 1) / s : n1[u];
+            if (steps > cost) cost = steps;
+        }
+        cost += kCombineSteps;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = KvSplit{s, U};
+        }
+    }
+    return best;
+}
+
+size_t split_part_o_bytes(int kv_split, int BH, int N, int d) {
+    const size_t b = static_cast<size_t>(kv_split) * BH * N * d * 4;
+    return (b + 255) & ~static_cast<size_t>(255);
+}
+
+size_t split_workspace_bytes(int kv_split, int BH, int N, int d) {
+    if (kv_split <= 1) return 0;
+    return split_part_o_bytes(kv_split, BH, N, d) + static_cast<size_t>(kv_split) * BH * N * 4;
+}
+
+int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
+             float scale, bool allow_split, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    int st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
+    if (st != ATTN_OK) return st;
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    attn_plan_t plan;
+    if ((st = attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan)) != ATTN_OK) return st;
+
+    const int BH = B * H;
+    const KvSplit split = allow_split ? choose_kv_split(plan, dev->num_sms, BH, N, causal) : KvSplit{1, 0};
+    const int kv_split = split.segs;
+    if (kv_split > 1) {
+        if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < split_workspace_bytes(kv_split, BH, N, d))
+            return ATTN_ERR_INVALID_ARG;
+    }
+    CUtensorMap tq, tk, tv;
+    if ((st = encode_rows_map(&tq, Q, BH, N, d, kBr)) != ATTN_OK || (st = encode_rows_map(&tk, K, BH, N, d, kBc)) != ATTN_OK ||
+        (st = encode_rows_map(&tv, V, BH, N, d, kBc)) != ATTN_OK)
+        return st;
+
+    FwdParams p;
+    p.O = static_cast<__nv_bfloat16*>(O);
+    p.LSE = LSE;
+    p.error_word = dev->error_word;
+    p.timeout_ns = kDefaultTimeoutNs;
+    p.N = N;
+    p.BH = BH;
+    p.num_q_tiles = (N + kBr - 1) / kBr;
+    p.num_kv_tiles = (N + kBc - 1) / kBc;
+    p.num_pairs = (p.num_q_tiles + 1) / 2;
+    p.num_units = plan.num_units;
+    p.heads_per_group = plan.heads_per_group;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.kv_split = kv_split;
+    p.split_units = split.units;
+    p.num_items = split.units * kv_split + (plan.num_units - split.units);
+    p.part_o = kv_split > 1 ? static_cast<float*>(workspace) : nullptr;
+    p.part_lse = kv_split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                         split_part_o_bytes(kv_split, BH, N, d))
+                              : nullptr;
+
+    if (d == 64)
+        return causal ? launch<64, true>(*dev, plan, tq, tk, tv, p, stream)
+                      : launch<64, false>(*dev, plan, tq, tk, tv, p, stream);
+    return causal ? launch<128, true>(*dev, plan, tq, tk, tv, p, stream)
+                  : launch<128, false>(*dev, plan, tq, tk, tv, p, stream);
 }
 
 }  // namespace
@@ -54,38 +193,23 @@ extern "C" int attn_plan(int B, int H, int N, int d, int causal, int num_sms, at
 
 extern "C" int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
                         int d, int causal, float scale, cudaStream_t stream) {
-    int st = check_args(Q, K, V, O, LSE, B, H, N, d, scale);
-    if (st != ATTN_OK) return st;
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, d, causal, scale, false, nullptr, 0, stream);
+}
+
+extern "C" size_t attn_fwd_split_workspace_bytes(int B, int H, int N, int d, int causal) {
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+    if (static_cast<long long>(B) * H * N >= (1ll << 31)) return 0;
     DeviceState* dev = nullptr;
-    if ((st = device_state(&dev)) != ATTN_OK) return st;
+    if (device_state(&dev) != ATTN_OK) return 0;
     attn_plan_t plan;
-    if ((st = attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan)) != ATTN_OK) return st;
+    if (attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan) != ATTN_OK) return 0;
+    return split_workspace_bytes(choose_kv_split(plan, dev->num_sms, B * H, N, causal).segs, B * H, N, d);
+}
 
-    const int BH = B * H;
-    CUtensorMap tq, tk, tv;
-    if ((st = encode_rows_map(&tq, Q, BH, N, d, kBr)) != ATTN_OK || (st = encode_rows_map(&tk, K, BH, N, d, kBc)) != ATTN_OK ||
-        (st = encode_rows_map(&tv, V, BH, N, d, kBc)) != ATTN_OK)
-        return st;
-
-    FwdParams p;
-    p.O = static_cast<__nv_bfloat16*>(O);
-    p.LSE = LSE;
-    p.error_word = dev->error_word;
-    p.timeout_ns = kDefaultTimeoutNs;
-    p.N = N;
-    p.BH = BH;
-    p.num_q_tiles = (N + kBr - 1) / kBr;
-    p.num_kv_tiles = (N + kBc - 1) / kBc;
-    p.num_pairs = (p.num_q_tiles + 1) / 2;
-    p.num_units = plan.num_units;
-    p.heads_per_group = plan.heads_per_group;
-    p.scale_log2 = scale * 1.4426950408889634f;
-
-    if (d == 64)
-        return causal ? launch<64, true>(*dev, plan, tq, tk, tv, p, stream)
-                      : launch<64, false>(*dev, plan, tq, tk, tv, p, stream);
-    return causal ? launch<128, true>(*dev, plan, tq, tk, tv, p, stream)
-                  : launch<128, false>(*dev, plan, tq, tk, tv, p, stream);
+extern "C" int attn_fwd_split(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                              int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+    return fwd_impl(Q, K, V, O, LSE, B, H, N, d, causal, scale, true, workspace, workspace_bytes, stream);
 }
 
 extern "C" size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d) {
@@ -363,6 +487,11 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, voi
     p.num_units = plan.num_units;
     p.heads_per_group = plan.heads_per_group;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.kv_split = 1;
+    p.split_units = 0;
+    p.num_items = plan.num_units;
+    p.part_o = nullptr;
+    p.part_lse = nullptr;
 
     if (d == 64) {
         if (causal)

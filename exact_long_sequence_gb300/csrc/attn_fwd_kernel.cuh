@@ -60,6 +60,16 @@ struct FwdParams {
     int heads_per_group;   // causal schedule only
     float scale_log2;      // scale * log2(e) (times the Q and K scales for the FP8 kernel)
     float out_scale;       // FP8 kernel: the V scale, applied with 1 / l; unused here
+    // K/V split (this kernel only; the FP8 kernel runs whole units): the first
+    // split_units units in schedule order are cut into kv_split segments of
+    // consecutive K/V tiles, one work item each; the other units are one item.
+    // A split item writes O / l and its LSE to part_o / part_lse, and
+    // attn_fwd_combine_kernel merges them.
+    int kv_split;          // segments per split unit (1: no split)
+    int split_units;       // units that are split (0: none)
+    int num_items;         // split_units * kv_split + (num_units - split_units)
+    float* part_o;         // [kv_split, BH, N, d] fp32
+    float* part_lse;       // [kv_split, BH, N] fp32 (natural log)
 };
 
 struct UnitInfo {
@@ -95,6 +105,54 @@ __device__ __forceinline__ UnitInfo decode_unit(int u, const FwdParams& p) {
         ui.n[t] = CAUSAL ? min(qt + 1, p.num_kv_tiles) : p.num_kv_tiles;
     }
     return ui;
+}
+
+constexpr int kMaxKvSplit = 4;
+
+// Work item w: segment `seg` of `nseg` of a unit, covering the pair's K/V tiles
+// [jb, je); tile t visits [jb, min(je, n[t])).  The host splits a unit into s
+// segments only when s (s - 1) < n[0]; with n[1] equal to n[0] or n[0] + 1 each
+// segment then holds at least one K/V tile of tile 0, so every row sees at
+// least one key in every segment.
+struct ItemInfo {
+    UnitInfo ui;
+    int seg;
+    int nseg;
+    int jb, je;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ ItemInfo decode_item(int w, const FwdParams& p) {
+    ItemInfo it;
+    const int head_items = p.split_units * p.kv_split;
+    int u;
+    if (w < head_items) {
+        u = w / p.kv_split;
+        it.seg = w - u * p.kv_split;
+        it.nseg = p.kv_split;
+    } else {
+        u = p.split_units + (w - head_items);
+        it.seg = 0;
+        it.nseg = 1;
+    }
+    it.ui = decode_unit<CAUSAL>(u, p);
+    const int n1 = it.ui.n[1];
+    const int c = (n1 + it.nseg - 1) / it.nseg;
+    it.jb = it.seg * c;
+    it.je = min(n1, it.jb + c);
+    return it;
+}
+
+// Inverse of decode_unit: the unit that holds query-tile pair `pair` of (batch,
+// head) bh.
+template <bool CAUSAL>
+__device__ __forceinline__ int unit_index(int bh, int pair, const FwdParams& p) {
+    if (!CAUSAL) return bh * p.num_pairs + pair;
+    const int G = p.heads_per_group;
+    const int g = bh / G;
+    const int heads_here = min(G, p.BH - g * G);
+    const int rank = p.num_pairs - 1 - pair;
+    return g * G * p.num_pairs + rank * heads_here + (bh - g * G);
 }
 
 // Position in the shared-memory K/V ring: stage index and the parity of the
@@ -178,6 +236,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // A split launch's combine kernel may be scheduled onto SMs as this grid's
+    // CTAs retire; it waits for this whole grid (griddepcontrol.wait) before it
+    // reads the partial results.
+    if (p.kv_split > 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -186,8 +248,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         uint32_t ul = 0;
         uint32_t q_issued = 0;    // bit t: a Q_t load of local unit (ul) is in flight
         bool ok = true;
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
-            const UnitInfo ui = decode_unit<CAUSAL>(u, p);
+        for (int w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+            const ItemInfo item = decode_item<CAUSAL>(w, p);
+            const UnitInfo& ui = item.ui;
             q_issued = 0;
             for (int t = 0; t < 2 && ok; ++t) {
                 ok = mbar_wait(bar(L::kQEmpty + t), (ul & 1u) ^ 1u, ctx);
@@ -199,8 +262,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     tma_load_3d(dst + b * (kBr * 128), &tmap_q, bar(L::kQFull + t), b * 64, (ui.q0 + t) * kBr, ui.bh);
                 q_issued |= 1u << t;
             }
-            const int n1 = ui.n[1];
-            for (int j = 0; j < n1 && ok; ++j) {
+            for (int j = item.jb; j < item.je && ok; ++j) {
 #pragma unroll
                 for (int kv = 0; kv < 2; ++kv) {
                     ok = mbar_wait(bar(L::kKvEmpty + pos.stage), pos.phase ^ 1u, ctx);
@@ -216,6 +278,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
             }
             if (!ok) break;
+            ++ul;
         }
         if (!ok) {
             // Abort: wait (bounded) for the copies still in flight before the
@@ -265,23 +328,24 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 mma_ts(tmem + 2 * kBc + t * D, tmem + t * kBc + kk * 8,
                        b + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_o, (accumulate || kk > 0) ? 1u : 0u);
         };
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
-            const UnitInfo ui = decode_unit<CAUSAL>(u, p);
-            const int n0 = ui.n[0], n1 = ui.n[1];
+        for (int w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+            const ItemInfo item = decode_item<CAUSAL>(w, p);
+            // K/V tiles [jb, e1) of the pair; tile 0 stops at e0 (causal: one earlier)
+            const int jb = item.jb, e1 = item.je, e0 = min(item.je, item.ui.n[0]);
             ok = mbar_wait(bar(L::kQFull + 0), ul & 1u, ctx) && mbar_wait(bar(L::kQFull + 1), ul & 1u, ctx);
             ok = __all_sync(0xffffffffu, ok);
             // O_t += P_t V_j with V_j at ring position `vp`, with the waits it needs.
             auto pv = [&](int t, int j, RingPos vp) -> bool {
                 bool w = true;
-                if (t == 0 || j >= n0)  // first use of V_j
+                if (t == 0 || j >= e0)  // first use of V_j
                     w = mbar_wait(bar(L::kKvFull + vp.stage), vp.phase, ctx);
                 // The softmax releases P_t in two halves, so the tensor core
                 // starts on keys 0-63 while the exponentials of 64-127 run.
                 w = w && mbar_wait(bar(L::kPHalf + t), p_phase[t], ctx);
-                if (j == 0) w = w && mbar_wait(bar(L::kOEmpty + t), (ul & 1u) ^ 1u, ctx);
+                if (j == jb) w = w && mbar_wait(bar(L::kOEmpty + t), (ul & 1u) ^ 1u, ctx);
                 if (!__all_sync(0xffffffffu, w)) return false;
                 tc_fence_after_sync();  // P_t and the O_t rescale came from other threads' tcgen05.st
-                if (elect_one()) gemm_o(t, vp.stage, 0, j > 0);
+                if (elect_one()) gemm_o(t, vp.stage, 0, j > jb);
                 __syncwarp();
                 w = mbar_wait(bar(L::kPFull + t), p_phase[t], ctx);
                 p_phase[t] ^= 1u;
@@ -290,38 +354,39 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (elect_one()) {
                     gemm_o(t, vp.stage, 1, true);
                     if (t == 1) mma_commit(bar(L::kKvEmpty + vp.stage));  // V_j's last reader
-                    if (j == ui.n[t] - 1) mma_commit(bar(L::kOFull + t));
+                    if (j == (t == 0 ? e0 : e1) - 1) mma_commit(bar(L::kOFull + t));
                 }
                 __syncwarp();
                 return true;
             };
             RingPos vpos = kpos.next(L::kStages);  // V_j
             RingPos vprev = vpos;                  // V_{j-1}
-            for (int j = 0; j < n1 && ok; ++j) {
+            for (int j = jb; j < e1 && ok; ++j) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(L::kKvFull + kpos.stage), kpos.phase, ctx));
                 if (!ok) break;
-                if (j < n0) {
+                if (j < e0) {
                     if (elect_one()) {
                         gemm_s(0, kpos.stage);
                         mma_commit(bar(L::kSFull + 0));
-                        if (j == n0 - 1) mma_commit(bar(L::kQEmpty + 0));
+                        if (j == e0 - 1) mma_commit(bar(L::kQEmpty + 0));
                     }
                     __syncwarp();
                 }
-                if (j > 0 && !(ok = pv(1, j - 1, vprev))) break;
+                if (j > jb && !(ok = pv(1, j - 1, vprev))) break;
                 if (elect_one()) {
                     gemm_s(1, kpos.stage);
                     mma_commit(bar(L::kSFull + 1));
                     mma_commit(bar(L::kKvEmpty + kpos.stage));  // K_j's last reader
-                    if (j == n1 - 1) mma_commit(bar(L::kQEmpty + 1));
+                    if (j == e1 - 1) mma_commit(bar(L::kQEmpty + 1));
                 }
                 __syncwarp();
-                if (j < n0 && !(ok = pv(0, j, vpos))) break;
+                if (j < e0 && !(ok = pv(0, j, vpos))) break;
                 vprev = vpos;
                 kpos = kpos.next(L::kStages).next(L::kStages);
                 vpos = vpos.next(L::kStages).next(L::kStages);
             }
-            if (ok) ok = pv(1, n1 - 1, vprev);
+            if (ok) ok = pv(1, e1 - 1, vprev);
+            ++ul;
         }
         // Make sure no MMA is still writing TMEM when it is released.
         if (elect_one()) mma_commit(bar(L::kDrain));
@@ -339,14 +404,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         uint32_t s_cnt = 0;
         uint32_t ul = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
-            const UnitInfo ui = decode_unit<CAUSAL>(u, p);
+        for (int w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+            const ItemInfo item = decode_item<CAUSAL>(w, p);
+            const UnitInfo& ui = item.ui;
             const int qt = ui.q0 + t;
             const int qrow = qt * kBr + rloc;
-            const int nt = ui.n[t];
+            const int jb = item.jb;
+            const int et = min(item.je, ui.n[t]);  // this tile's K/V tiles are [jb, et)
             float m_ref = -INFINITY;
             float l = 0.f;
-            for (int j = 0; j < nt; ++j) {
+            for (int j = jb; j < et; ++j) {
                 ok = mbar_wait(bar(L::kSFull + t), s_cnt & 1u, ctx);
                 ++s_cnt;
                 __syncwarp();
@@ -435,7 +502,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 // before the first half of P_t is released to O_t += P_t V.
                 // O_t's previous P V has completed: it was issued before this
                 // S_t, whose completion was just observed.
-                if (__any_sync(0xffffffffu, grow && j > 0)) {
+                if (__any_sync(0xffffffffu, grow && j > jb)) {
 #pragma unroll 1
                     for (int c = 0; c < D; c += 32) {
                         uint32_t o[32];
@@ -465,28 +532,46 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const float inv_l = 1.f / l;
             const bool row_ok = qrow < p.N;
             const size_t grow_idx = static_cast<size_t>(ui.bh) * p.N + (row_ok ? qrow : 0);
-            uint4* orow = reinterpret_cast<uint4*>(p.O + grow_idx * D);
+            const float lse = ((m_ref == -INFINITY ? 0.f : m_ref) + lg2_approx(l)) * kLn2;
+            if (item.nseg == 1) {
+                uint4* orow = reinterpret_cast<uint4*>(p.O + grow_idx * D);
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(t_o + c, o);
-                tmem_wait_ld(o);
-                uint32_t w[16];
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c, o);
+                    tmem_wait_ld(o);
+                    uint32_t pw[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (row_ok) {
+                    for (int i = 0; i < 16; ++i)
+                        pw[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                    if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        orow[c / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i)
+                            orow[c / 8 + i] = make_uint4(pw[4 * i], pw[4 * i + 1], pw[4 * i + 2], pw[4 * i + 3]);
+                    }
                 }
-            }
-            if (row_ok) {
-                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                p.LSE[grow_idx] = (m_use + lg2_approx(l)) * kLn2;
+                if (row_ok) p.LSE[grow_idx] = lse;
+            } else {
+                // this segment's O / l (fp32) and LSE, merged later by the combine kernel
+                const size_t pidx = static_cast<size_t>(item.seg) * p.BH * p.N + grow_idx;
+                float4* orow = reinterpret_cast<float4*>(p.part_o + pidx * D);
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c, o);
+                    tmem_wait_ld(o);
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            orow[c / 4 + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                                          __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+                    }
+                }
+                if (row_ok) p.part_lse[pidx] = lse;
             }
             tc_fence_before_sync();
             mbar_arrive(bar(L::kOEmpty + t));
+            ++ul;
         }
     }
 
@@ -496,6 +581,58 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Merge the segments of the split units: per row, with the segments' partial
+// results (O_s = softmax over the segment's keys times V, LSE_s),
+//     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
+// the same online-softmax combination as inside the kernel, across segments.
+// One warp per row; rows of unsplit units were written by the kernel itself.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256) attn_fwd_combine_kernel(const FwdParams p) {
+    constexpr int kPer = D / 32;  // columns per lane
+    // launched as a programmatic dependent of the attention kernel: wait until
+    // that grid has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const size_t rows = static_cast<size_t>(p.BH) * p.N;
+    const size_t row = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int bh = static_cast<int>(row / static_cast<size_t>(p.N));
+    const int i = static_cast<int>(row - static_cast<size_t>(bh) * p.N);
+    if (unit_index<CAUSAL>(bh, i / kBr / 2, p) >= p.split_units) return;
+    const int nseg = p.kv_split;
+    const size_t seg_stride = rows;
+    float lse[kMaxKvSplit];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) {
+        lse[s] = s < nseg ? p.part_lse[s * seg_stride + row] : -INFINITY;
+        mx = fmaxf(mx, lse[s]);
+    }
+    float wsum = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) {
+        lse[s] = s < nseg ? expf(lse[s] - mx) : 0.f;  // now the segment weights
+        wsum += lse[s];
+    }
+    const float inv = 1.f / wsum;
+    float acc[kPer];
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) {
+        if (s < nseg) {
+            const float* src = p.part_o + (s * seg_stride + row) * D + lane * kPer;
+            const float ws = lse[s] * inv;
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) acc[c] = fmaf(ws, src[c], acc[c]);
+        }
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(p.O + row * D + lane * kPer);
+#pragma unroll
+    for (int c = 0; c < kPer; c += 2) dst[c / 2] = pack_bf16x2(acc[c], acc[c + 1]);
+    if (lane == 0) p.LSE[row] = mx + logf(wsum);
 }
 
 }  // namespace elsattn

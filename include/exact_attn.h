@@ -106,6 +106,33 @@ int attn_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh, floa
 size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
 
 /*
+ * attn_fwd_split - attn_fwd that may also cut the K/V range of long units into
+ * segments, for problems with fewer work units than SMs (few heads, or a
+ * causal mask whose longest query tiles dominate).  Each segment is a work
+ * item of its own; it writes its partial result (O over the segment's keys,
+ * normalised, fp32, and that segment's LSE) to `workspace`, and a second
+ * kernel on `stream` merges the segments of each row by
+ *     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
+ * the combination step of the online softmax ("streaming reformulation" of the
+ * IO-Aware Algorithms page) applied across segments.  The result is the same
+ * operation as attn_fwd, up to floating-point rounding.
+ *   arguments as attn_fwd, plus
+ *   workspace       : device buffer of at least attn_fwd_split_workspace_bytes()
+ *                     bytes, 16-byte aligned, owned by the caller; may be NULL
+ *                     when that size is 0 (no split pays: this call then runs
+ *                     exactly attn_fwd)
+ *   workspace_bytes : its size
+ * Returns ATTN_ERR_INVALID_ARG when a split is chosen and the workspace is
+ * missing, misaligned or too small; otherwise as attn_fwd.
+ */
+int attn_fwd_split(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
+                   int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes attn_fwd_split needs on the current device; 0 when it would
+ * not split (or the shape is invalid). */
+size_t attn_fwd_split_workspace_bytes(int B, int H, int N, int d, int causal);
+
+/*
  * attn_bwd - gradients of attn_fwd for an upstream gradient dO of O:
  *     dV = P^T dO,  dS = P * (dO V^T - D) with D_i = sum_c dO_ic O_ic,
  *     dQ = scale * dS K,  dK = scale * dS^T Q,

@@ -119,6 +119,16 @@ def test_host_entry_validation_and_workspace_size(lib):
     assert lib.attn_debug_wait_timeout(11_000_000_000, None) == ela.ATTN_ERR_INVALID_ARG
 
 
+def test_split_entry_validation(lib):
+    """attn_fwd_split checks its tensor arguments like attn_fwd; its size query is 0 for invalid shapes."""
+    for shape in ((0, 1, 128, 64), (1, 1, 0, 64), (1, 1, 128, 96), (1 << 16, 1 << 8, 1 << 8, 64)):
+        assert lib.attn_fwd_split_workspace_bytes(*shape, 1) == 0
+    args = (0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 1, 1, 128, 96, 0, 0.125)
+    assert lib.attn_fwd_split(*args, None, 0, None) in (ela.ATTN_ERR_INVALID_ARG, ela.ATTN_ERR_UNSUPPORTED)
+    args = (0x1000, 0x2008, 0x3000, 0x4000, 0x5000, 1, 1, 128, 64, 0, 0.125)
+    assert lib.attn_fwd_split(*args, None, 0, None) == ela.ATTN_ERR_MISALIGNED
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_valid_call_without_gpu_reports_no_device(lib):
     assert call_fwd(lib) in (ela.ATTN_ERR_NO_DEVICE, ela.ATTN_ERR_CUDA)

@@ -1,0 +1,150 @@
+"""GPU parity of the K/V split (attn_fwd_split).
+
+Problems with fewer work units than SMs cut the K/V range of their long units
+into segments that run on different CTAs; a second kernel merges the segments'
+partial results of each row by their LSE weights.  The result is the same
+operation as attn_fwd, so the forward's tolerances apply unchanged: against the
+fp64 oracle max |dO| <= 2e-2 and per-row |dLSE| <= 1e-3 |LSE|.  The shapes below
+are chosen so that the launch splits units into 2, 3 and 4 segments on a
+152-SM GB300 (the test reads the split the library chose back from the
+workspace size and checks it is the expected one), with causal masks, ragged
+lengths, several schedule groups, and units left whole beside split ones.
+"""
+import pytest
+import torch
+
+import exact_long_sequence_gb300 as ela
+from exact_long_sequence_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from exact_long_sequence_gb300 import _build
+
+    _build.build()
+    ela.load_library()
+
+
+def chosen_split(B, H, N, d, causal):
+    """Segments per split unit, recovered from the workspace size (1: no split)."""
+    need = ela.split_workspace_bytes(B, H, N, d, causal)
+    if need == 0:
+        return 1
+    rows = B * H * N
+    for s in range(2, 5):
+        if ((s * rows * d * 4 + 255) // 256) * 256 + s * rows * 4 == need:
+            return s
+    raise AssertionError(f"workspace size {need} matches no split factor")
+
+
+# (B, H, N, d, causal, segments per split unit expected on 152 SMs).  Only the
+# heaviest units, as many as the idle SMs allow, are split; the rest run whole.
+CASES = [
+    (1, 8, 4096, 64, True, 2),     # the causal d = 64 workload: 128 units, the 24 heaviest split
+    (1, 2, 8192, 128, False, 2),   # 64 equal units, all split
+    (1, 1, 1000, 64, False, 3),    # 4 units of 8 K/V tiles, ragged length
+    (1, 5, 3000, 64, True, 3),     # ragged causal, 60 units of which 45 split
+    (2, 1, 2000, 128, True, 3),    # ragged causal, two batches in two schedule groups
+    (1, 1, 4096, 128, False, 4),   # 16 units of 32 K/V tiles
+    (1, 1, 8192, 64, True, 4),     # causal, 32 units of which 26 split
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,segs", CASES)
+def test_split_parity(oracle_mod, B, H, N, d, causal, segs):
+    needs_152_sms()
+    assert chosen_split(B, H, N, d, causal) == segs
+    q, k, v = workloads.make_inputs(B, H, N, d, seed=900 + N + H)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = ela.attn_fwd(qd, kd, vd, causal=causal)
+    o1, lse1 = ela.attn_fwd(qd, kd, vd, causal=causal, split=False)
+    torch.cuda.synchronize()
+    assert ela.last_device_error() == ela.ATTN_OK
+    # every row of the small cases, sampled rows (with the first and last) of the long ones
+    R = N if B * H * N <= 16384 else 48
+    rows = None
+    if R < N:
+        rows = workloads.sample_rows(B * H, N, R - 2, seed=N)
+        ends = torch.tensor([[0, N - 1]]).repeat(B * H, 1)
+        rows = torch.cat([ends, rows], dim=1).sort(dim=1).values
+    O_ref, L_ref = oracle_mod.attention_rows(q, k, v, causal, ela.default_scale(d),
+                                             rows=None if rows is None else rows.numpy())
+    for out, lout, label in ((o, lse, "split"), (o1, lse1, "unsplit")):
+        oo = out.reshape(B * H, N, d)
+        ll = lout.reshape(B * H, N)
+        if rows is not None:
+            idx = rows.cuda()
+            oo = torch.gather(oo, 1, idx[:, :, None].expand(-1, -1, d))
+            ll = torch.gather(ll, 1, idx)
+        oo = oo.double().cpu().numpy()
+        ll = ll.double().cpu().numpy()
+        err = abs(oo - O_ref).max()
+        rel = (abs(ll - L_ref) / abs(L_ref)).max()
+        assert err <= O_TOL, f"{label}: max|dO| = {err:.3e}"
+        assert rel <= 1e-3, f"{label}: max rel dLSE = {rel:.3e}"
+    # the split and the single kernel agree to the bf16 output's rounding
+    assert (o.float() - o1.float()).abs().max().item() <= 2 ** -7 * max(1.0, o1.float().abs().max().item())
+
+
+def test_no_split_when_it_would_not_pay():
+    """More units than SMs (the long-sequence workloads), or equal units that the idle SMs
+    cannot all split: attn_fwd_split is attn_fwd."""
+    needs_152_sms()
+    assert ela.split_workspace_bytes(1, 16, 16384, 128, False) == 0
+    assert ela.split_workspace_bytes(1, 8, 65536, 128, True) == 0
+    assert ela.split_workspace_bytes(1, 8, 4096, 64, False) == 0
+    assert ela.split_workspace_bytes(1, 1, 256, 64, False) == 0
+
+
+def needs_152_sms():
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the shapes split on 152 SMs")
+
+
+def test_split_rejects_a_missing_or_short_workspace():
+    needs_152_sms()
+    lib = ela.load_library()
+    B, H, N, d = 1, 8, 4096, 64
+    need = ela.split_workspace_bytes(B, H, N, d, True)
+    assert need > 0
+    q = torch.zeros(B, H, N, d, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    ws = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
+    args = (q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, 1, 0.125)
+    assert lib.attn_fwd_split(*args, None, 0, None) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_split(*args, ws.data_ptr(), need - 1, None) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_split(*args, ws.data_ptr() + 4, need, None) == ela.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_split(*args, ws.data_ptr(), need, None) == ela.ATTN_OK
+    torch.cuda.synchronize()
+    assert ela.last_device_error() == ela.ATTN_OK
+    # no split for this shape: a NULL workspace is accepted
+    small = (q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 256, d, 0, 0.125)
+    assert ela.split_workspace_bytes(1, 1, 256, d, False) == 0
+    assert lib.attn_fwd_split(*small, None, 0, None) == ela.ATTN_OK
+    torch.cuda.synchronize()
+
+
+def test_split_stays_inside_its_buffers():
+    """Guard canaries after O, LSE and the workspace stay untouched by a split launch."""
+    needs_152_sms()
+    B, H, N, d = 1, 5, 3000, 64
+    need = ela.split_workspace_bytes(B, H, N, d, True)
+    assert need > 0
+    q, k, v = (t.cuda() for t in workloads.make_inputs(B, H, N, d, seed=5))
+    o_buf = torch.full((B * H * N * d + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((B * H * N + 1024,), 7.0, dtype=torch.float32, device="cuda")
+    w_buf = torch.full((need + 8192,), 0x5A, dtype=torch.uint8, device="cuda")
+    o = o_buf[: B * H * N * d].view(B, H, N, d)
+    lse = l_buf[: B * H * N].view(B, H, N)
+    ela.attn_fwd(q, k, v, causal=True, out=o, lse=lse, workspace=w_buf[:need])
+    torch.cuda.synchronize()
+    assert ela.last_device_error() == ela.ATTN_OK
+    assert (o_buf[B * H * N * d:] == 7.0).all() and (l_buf[B * H * N:] == 7.0).all()
+    assert (w_buf[need:] == 0x5A).all()
