@@ -55,6 +55,15 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "sm103_ptx.cuh", "plan.h", "plan.cpp", "attn_api.cu"]
+# The sources each pass's recorded traffic depends on: an entry of the traffic file is used only
+# while their hash is the one it was captured with.
+PASS_SOURCES = {
+    "fwd": KERNEL_SOURCES,
+    "fp8": ["attn_fwd_fp8_kernel.cuh", "attn_fwd_kernel.cuh", "sm103_ptx.cuh", "plan.h", "plan.cpp",
+            "attn_fp8_api.cu"],
+    "bwd": ["attn_bwd_kernel.cuh", "sm103_ptx.cuh", "sm103_bulk.cuh", "plan.h", "attn_bwd_api.cu"],
+    "rows": ["rowwise_kernels.cuh", "rowwise_api.cu"],
+}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -110,24 +119,24 @@ def read_peaks():
         return FALLBACK_BF16_TFLOPS, None, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kind: str = "fwd") -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in PASS_SOURCES[kind]:
         with open(os.path.join(ROOT, "exact_long_sequence_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu capture, or None if the
-    kernel sources changed since it was taken (or there is none)."""
+def recorded_traffic(key: str, kind: str = "fwd"):
+    """DRAM bytes per launch (per step for two-launch row passes) from the committed ncu
+    capture, or None if the pass's kernel sources changed since it was taken (or there is none)."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    entry = rec.get(workload)
-    if not entry or entry.get("kernel_source_sha256") != kernel_source_hash():
+    entry = rec.get(key)
+    if not entry or entry.get("kernel_source_sha256") != kernel_source_hash(kind):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -395,7 +404,8 @@ def run_gb300_fp8(args, w):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                 "peak_kind": (f"{peak_kind} dense bf16 burst (MEASURED_PEAKS.json) x 2, the nominal FP8/BF16 "
                               "tensor ratio (4.5 / 2.25 PFLOP/s)"),
-                "traffic": None, "algorithmic_flops_per_launch": w.flops, "kernel_ms": kernel_ms,
+                "traffic": recorded_traffic("fp8:" + w.name, "fp8"), "algorithmic_flops_per_launch": w.flops,
+                "kernel_ms": kernel_ms,
                 "note": "step = the V transpose and the attention kernel; the step time is used for both",
                 "frac_of_bf16_peak": achieved / peak_bf16}
     if peak_bf16_sustained:
@@ -530,7 +540,8 @@ def run_gb300_rows(args, kind):
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)",
                    "parallelism": "replicas", "reads_of_x_per_step": passes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json)", "traffic": None,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json)",
+                     "traffic": recorded_traffic(name, "rows"),
                      "algorithmic_bytes_per_launch": alg_bytes, "kernel_ms": kernel_ms},
         "gpu_launches": args.steps * (1 if passes == 1 else 2), "clocks": clocks.summary(),
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
@@ -608,8 +619,10 @@ def run_gb300_bwd(args, w):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} dense bf16 burst (MEASURED_PEAKS.json)" if peak_kind == "measured"
                 else "fallback dense bf16 burst",
-                "traffic": None, "algorithmic_flops_per_launch": flops, "kernel_ms": kernel_ms,
-                "note": "step = the three launches of attn_bwd (row statistics, gradients, dQ to bf16)"}
+                "traffic": recorded_traffic("bwd:" + w.name, "bwd"), "algorithmic_flops_per_launch": flops,
+                "kernel_ms": kernel_ms,
+                "note": ("step = the three launches of attn_bwd (row statistics, gradients, dQ to bf16); "
+                         "traffic is the gradient kernel's")}
     if peak_sustained:
         roofline["frac_of_sustained"] = achieved / peak_sustained
     line = {
