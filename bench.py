@@ -681,9 +681,11 @@ def run_gb300(args, w):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     # Workloads with fewer work units than SMs take the K/V split (attention kernel + combine
     # kernel); its workspace is allocated once, outside the timed region.
+    # Causal workloads with more units than SMs take the dynamic schedule (a counter in the
+    # same workspace, zeroed by a memset on the stream before each launch).
     split_bytes = ela.split_workspace_bytes(w.B, w.H, w.N, w.d, w.causal)
     split_ws = torch.empty(split_bytes, dtype=torch.uint8, device=dev) if split_bytes else None
-    launches_per_step = 2 if split_bytes else 1
+    launches_per_step = 2 if ela.split_segments(w.B, w.H, w.N, w.d, w.causal) > 1 else 1
 
     for _ in range(max(3, args.warmup)):
         ela.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream, workspace=split_ws)
@@ -756,7 +758,7 @@ def run_gb300(args, w):
                 "traffic": recorded_traffic(w.name),
                 "algorithmic_flops_per_launch": w.flops, "kernel_ms": kernel_ms,
                 "io_bound_bytes": w.io_bytes}
-    if split_bytes:
+    if launches_per_step == 2:
         roofline["note"] = ("K/V split: the step is the attention kernel plus the combine kernel; "
                             "the step time is used for both")
     if peak_sustained:

@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "attn_fwd_host_workspace_bytes",
     "attn_fwd_split",
     "attn_fwd_split_workspace_bytes",
+    "attn_fwd_split_segments",
     "attn_plan",
     "attn_last_device_error",
     "attn_last_cuda_error",
@@ -102,6 +103,8 @@ def load_library(path: str | None = None):
     lib.attn_fwd_split.restype = i
     lib.attn_fwd_split_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.attn_fwd_split_workspace_bytes.restype = ctypes.c_size_t
+    lib.attn_fwd_split_segments.argtypes = [i, i, i, i, i]
+    lib.attn_fwd_split_segments.restype = i
     lib.attn_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(AttnPlan)]
     lib.attn_plan.restype = i
     lib.attn_last_device_error.argtypes = [vp]
@@ -154,8 +157,13 @@ def _stream_handle(stream):
 
 
 def split_workspace_bytes(B: int, H: int, N: int, d: int, causal: bool) -> int:
-    """Device bytes attn_fwd_split needs for this shape on the current device (0: it would not split)."""
+    """Device bytes attn_fwd_split needs for this shape on the current device (0: none)."""
     return int(load_library().attn_fwd_split_workspace_bytes(B, H, N, d, int(bool(causal))))
+
+
+def split_segments(B: int, H: int, N: int, d: int, causal: bool) -> int:
+    """K/V segments per split unit attn_fwd_split chooses (1: no split; 0: invalid or no device)."""
+    return int(load_library().attn_fwd_split_segments(B, H, N, d, int(bool(causal))))
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
@@ -165,8 +173,8 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     q, k, v   : bf16 CUDA tensors [B, H, N, d], contiguous, d in {64, 128}
     out       : optional bf16 [B, H, N, d] output buffer; lse: optional fp32 [B, H, N]
     stream    : torch.cuda.Stream (default: the current stream); the call is asynchronous.
-    split     : allow the K/V split of attn_fwd_split for problems with fewer work units than
-                SMs (False: always the single-kernel attn_fwd)
+    split     : allow attn_fwd_split: the K/V split for problems with fewer work units than SMs,
+                and the dynamic schedule for causal problems with more (False: always attn_fwd)
     workspace : optional uint8 CUDA tensor of at least split_workspace_bytes() bytes for the
                 split (allocated here when needed and not given)
     """

@@ -19,7 +19,7 @@ struct DeviceState {
     int num_sms = 0;
     int cc_major = 0, cc_minor = 0;
     uint32_t* error_word = nullptr;  // 256-byte device block, first word = error code
-    bool smem_configured[2][2] = {{false, false}, {false, false}};      // forward <d == 128><causal>
+    bool smem_configured[2][2][2] = {};                                   // forward <d == 128><causal><dynamic schedule>
     bool bwd_smem_configured[2][2] = {{false, false}, {false, false}};  // backward <d == 128><causal>
     bool fp8_smem_configured[2] = {false, false};                         // FP8 forward <causal>
 };

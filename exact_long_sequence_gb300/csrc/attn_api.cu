@@ -20,11 +20,15 @@ extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sm
 namespace elsattn {
 namespace {
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DYN = false>
 int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, const CUtensorMap& tk,
            const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream) {
-    auto kernel = attn_fwd_kernel<D, CAUSAL>;
-    bool& configured = dev.smem_configured[D == 128][CAUSAL];
+    if constexpr (CAUSAL && !DYN) {
+        // causal launches with a schedule counter take the dynamic instantiation
+        if (p.sched_counter != nullptr) return launch<D, CAUSAL, true>(dev, plan, tq, tk, tv, p, stream);
+    }
+    auto kernel = attn_fwd_kernel<D, CAUSAL, DYN>;
+    bool& configured = dev.smem_configured[D == 128][CAUSAL][DYN];
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.smem_bytes);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -116,14 +120,26 @@ KvSplit choose_kv_split(const attn_plan_t& plan, int num_sms, int BH, int N, int
     return best;
 }
 
+// Dynamic work-item schedule (FwdParams::sched_counter): for causal launches
+// with more units than SMs, whose units differ in length, so that a static
+// stride would leave some CTAs with more work than others.
+bool use_dynamic_schedule(const attn_plan_t& plan, int num_sms, int causal) {
+    return causal && plan.num_units > num_sms;
+}
+
+// Workspace of attn_fwd_split: [256 B: the schedule counter][O partials][LSE partials].
+constexpr size_t kCounterBlock = 256;
+
 size_t split_part_o_bytes(int kv_split, int BH, int N, int d) {
     const size_t b = static_cast<size_t>(kv_split) * BH * N * d * 4;
     return (b + 255) & ~static_cast<size_t>(255);
 }
 
-size_t split_workspace_bytes(int kv_split, int BH, int N, int d) {
-    if (kv_split <= 1) return 0;
-    return split_part_o_bytes(kv_split, BH, N, d) + static_cast<size_t>(kv_split) * BH * N * 4;
+size_t split_workspace_bytes(int kv_split, bool dynamic, int BH, int N, int d) {
+    if (kv_split <= 1 && !dynamic) return 0;
+    size_t b = kCounterBlock;
+    if (kv_split > 1) b += split_part_o_bytes(kv_split, BH, N, d) + static_cast<size_t>(kv_split) * BH * N * 4;
+    return b;
 }
 
 int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
@@ -138,10 +154,10 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     const int BH = B * H;
     const KvSplit split = allow_split ? choose_kv_split(plan, dev->num_sms, BH, N, causal) : KvSplit{1, 0};
     const int kv_split = split.segs;
-    if (kv_split > 1) {
-        if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < split_workspace_bytes(kv_split, BH, N, d))
-            return ATTN_ERR_INVALID_ARG;
-    }
+    const bool dynamic = allow_split && use_dynamic_schedule(plan, dev->num_sms, causal);
+    const size_t need = split_workspace_bytes(kv_split, dynamic, BH, N, d);
+    if (need > 0 && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need))
+        return ATTN_ERR_INVALID_ARG;
     CUtensorMap tq, tk, tv;
     if ((st = encode_rows_map(&tq, Q, BH, N, d, kBr)) != ATTN_OK || (st = encode_rows_map(&tk, K, BH, N, d, kBc)) != ATTN_OK ||
         (st = encode_rows_map(&tv, V, BH, N, d, kBc)) != ATTN_OK)
@@ -163,10 +179,15 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     p.kv_split = kv_split;
     p.split_units = split.units;
     p.num_items = split.units * kv_split + (plan.num_units - split.units);
-    p.part_o = kv_split > 1 ? static_cast<float*>(workspace) : nullptr;
-    p.part_lse = kv_split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                         split_part_o_bytes(kv_split, BH, N, d))
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.part_o = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock) : nullptr;
+    p.part_lse = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + split_part_o_bytes(kv_split, BH, N, d))
                               : nullptr;
+    p.sched_counter = dynamic ? reinterpret_cast<int*>(ws) : nullptr;
+    if (dynamic) {
+        cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
 
     if (d == 64)
         return causal ? launch<64, true>(*dev, plan, tq, tk, tv, p, stream)
@@ -203,7 +224,18 @@ extern "C" size_t attn_fwd_split_workspace_bytes(int B, int H, int N, int d, int
     if (device_state(&dev) != ATTN_OK) return 0;
     attn_plan_t plan;
     if (attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan) != ATTN_OK) return 0;
-    return split_workspace_bytes(choose_kv_split(plan, dev->num_sms, B * H, N, causal).segs, B * H, N, d);
+    return split_workspace_bytes(choose_kv_split(plan, dev->num_sms, B * H, N, causal).segs,
+                                 use_dynamic_schedule(plan, dev->num_sms, causal), B * H, N, d);
+}
+
+extern "C" int attn_fwd_split_segments(int B, int H, int N, int d, int causal) {
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+    if (static_cast<long long>(B) * H * N >= (1ll << 31)) return 0;
+    DeviceState* dev = nullptr;
+    if (device_state(&dev) != ATTN_OK) return 0;
+    attn_plan_t plan;
+    if (attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan) != ATTN_OK) return 0;
+    return choose_kv_split(plan, dev->num_sms, B * H, N, causal).segs;
 }
 
 extern "C" int attn_fwd_split(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
@@ -492,6 +524,7 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, voi
     p.num_items = plan.num_units;
     p.part_o = nullptr;
     p.part_lse = nullptr;
+    p.sched_counter = nullptr;
 
     if (d == 64) {
         if (causal)

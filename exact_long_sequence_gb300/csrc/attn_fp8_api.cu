@@ -136,6 +136,7 @@ extern "C" int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void
     p.num_items = plan.num_units;
     p.part_o = nullptr;
     p.part_lse = nullptr;
+    p.sched_counter = nullptr;
     p.out_scale = v_scale;
     return causal ? launch_fp8<true>(*dev, plan, tq, tk, tvt, p, stream)
                   : launch_fp8<false>(*dev, plan, tq, tk, tvt, p, stream);

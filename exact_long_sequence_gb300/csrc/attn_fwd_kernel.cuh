@@ -70,6 +70,12 @@ struct FwdParams {
     int num_items;         // split_units * kv_split + (num_units - split_units)
     float* part_o;         // [kv_split, BH, N, d] fp32
     float* part_lse;       // [kv_split, BH, N] fp32 (natural log)
+    // Dynamic work-item schedule (kernel instantiated with DYN): each CTA starts
+    // with item blockIdx.x and then claims the next unclaimed item from this
+    // counter (zero at launch), so items go out in schedule order to whichever
+    // CTA is free first.  Static schedule (nullptr): CTA b takes items b,
+    // b + grid, b + 2 grid, ...
+    int* sched_counter;
 };
 
 struct UnitInfo {
@@ -155,6 +161,10 @@ __device__ __forceinline__ int unit_index(int bh, int pair, const FwdParams& p) 
     return g * G * p.num_pairs + rank * heads_here + (bh - g * G);
 }
 
+// The producer hands each CTA's work items to the other roles through a ring of
+// this many shared-memory slots (an item index, -1 at the end).
+constexpr int kItemRing = 2;
+
 // Position in the shared-memory K/V ring: stage index and the parity of the
 // stage's current fill.
 struct RingPos {
@@ -183,14 +193,19 @@ struct SmemLayout {
     static constexpr int kOFull = kPFull + 2;           // [2]
     static constexpr int kOEmpty = kOFull + 2;          // [2]
     static constexpr int kDrain = kOEmpty + 2;
-    static constexpr int kNumBars = kDrain + 1;
-    static constexpr int kFlagsOff = kBarOff + kNumBars * 8;  // tmem base slot, abort flag
+    static constexpr int kItemFull = kDrain + 1;        // [kItemRing] the slot holds the next item index
+    static constexpr int kItemEmpty = kItemFull + kItemRing;  // [kItemRing] MMA warp + 8 softmax warps read it
+    static constexpr int kNumBars = kItemEmpty + kItemRing;
+    static constexpr int kFlagsOff = kBarOff + kNumBars * 8;  // tmem base slot, abort flag, item indices
+    static constexpr int kItemOff = kFlagsOff + 8;             // [kItemRing] int
     static constexpr int kBytes = kFlagsOff + 16;
     static_assert(kNumBars == 2 * kStages + kFixedBarriers, "barrier count differs from the plan");
     static_assert(kBytes + kSmemAlign <= smem_bytes_for(D), "shared memory layout exceeds the plan");
 };
 
-template <int D, bool CAUSAL>
+// DYN: the dynamic work-item schedule (p.sched_counter is set); without it the
+// static schedule is compiled with no trace of the item ring.
+template <int D, bool CAUSAL, bool DYN = false>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
@@ -223,6 +238,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             mbar_init(bar(L::kOEmpty + t), 128);
         }
         mbar_init(bar(L::kDrain), 1);
+        for (int s = 0; s < kItemRing; ++s) {
+            mbar_init(bar(L::kItemFull + s), 1);
+            mbar_init(bar(L::kItemEmpty + s), 9);
+        }
         fence_barrier_init();
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
@@ -240,6 +259,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     // CTAs retire; it waits for this whole grid (griddepcontrol.wait) before it
     // reads the partial results.
     if (p.kv_split > 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kItemOff);
+    // Every role starts with item blockIdx.x (the grid never exceeds the item
+    // count).  The static schedule then advances by gridDim.x; the dynamic one
+    // takes the next items from the producer's ring: ring entry r is this CTA's
+    // item r + 1, or -1 after the last.  Consumer side (a whole warp calls it):
+    auto take_item = [&](uint32_t r, int& w) -> bool {
+        const uint32_t s = r % kItemRing;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(bar(L::kItemFull + s), (r / kItemRing) & 1u, ctx));
+        if (!got) return false;
+        w = item_slot[s];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kItemEmpty + s));
+        return true;
+    };
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -248,10 +281,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         uint32_t ul = 0;
         uint32_t q_issued = 0;    // bit t: a Q_t load of local unit (ul) is in flight
         bool ok = true;
-        for (int w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+        uint32_t r = 0;  // dynamic schedule: ring entries published
+        for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok;) {
+            q_issued = 0;
             const ItemInfo item = decode_item<CAUSAL>(w, p);
             const UnitInfo& ui = item.ui;
-            q_issued = 0;
             for (int t = 0; t < 2 && ok; ++t) {
                 ok = mbar_wait(bar(L::kQEmpty + t), (ul & 1u) ^ 1u, ctx);
                 if (!ok) break;
@@ -279,6 +313,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             }
             if (!ok) break;
             ++ul;
+            if constexpr (DYN) {
+                // claim this CTA's next item and publish it to the other roles
+                w = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
+                if (w >= p.num_items) w = -1;
+                const uint32_t s = r % kItemRing;
+                if (r >= kItemRing && !(ok = mbar_wait(bar(L::kItemEmpty + s), ((r / kItemRing) - 1) & 1u, ctx)))
+                    break;
+                item_slot[s] = w;
+                mbar_arrive(bar(L::kItemFull + s));
+                ++r;
+            } else {
+                w += gridDim.x;
+            }
         }
         if (!ok) {
             // Abort: wait (bounded) for the copies still in flight before the
@@ -328,7 +375,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 mma_ts(tmem + 2 * kBc + t * D, tmem + t * kBc + kk * 8,
                        b + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc_o, (accumulate || kk > 0) ? 1u : 0u);
         };
-        for (int w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+        uint32_t r = 0;
+        for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok;) {
             const ItemInfo item = decode_item<CAUSAL>(w, p);
             // K/V tiles [jb, e1) of the pair; tile 0 stops at e0 (causal: one earlier)
             const int jb = item.jb, e1 = item.je, e0 = min(item.je, item.ui.n[0]);
@@ -387,6 +435,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             }
             if (ok) ok = pv(1, e1 - 1, vprev);
             ++ul;
+            if constexpr (DYN) {
+                if (ok) ok = take_item(r++, w);
+            } else {
+                w += gridDim.x;
+            }
         }
         // Make sure no MMA is still writing TMEM when it is released.
         if (elect_one()) mma_commit(bar(L::kDrain));
@@ -404,7 +457,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         uint32_t s_cnt = 0;
         uint32_t ul = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < p.num_items && ok; w += gridDim.x) {
+        uint32_t r = 0;
+        for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok;) {
             const ItemInfo item = decode_item<CAUSAL>(w, p);
             const UnitInfo& ui = item.ui;
             const int qt = ui.q0 + t;
@@ -572,6 +626,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             tc_fence_before_sync();
             mbar_arrive(bar(L::kOEmpty + t));
             ++ul;
+            if constexpr (DYN) {
+                ok = take_item(r++, w);
+            } else {
+                w += gridDim.x;
+            }
         }
     }
 

@@ -18,8 +18,8 @@ constexpr int kThreads = 384;     // warp 0 TMA, warp 1 MMA, warps 4-7 / 8-11 so
 constexpr int kTmemCols = 512;    // S0 | S1 | O0 | O1 (P aliases the first half of S)
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per CTA on sm_100-family SMs
 constexpr int kSmemAlign = 1024;    // slack to align the tiles to the 1024-byte swizzle atom
-constexpr int kFixedBarriers = 15;  // mbarriers besides the two per K/V stage
-constexpr int kFlagBytes = 16;      // TMEM base address slot and abort flag
+constexpr int kFixedBarriers = 19;  // mbarriers besides the two per K/V stage
+constexpr int kFlagBytes = 16;      // TMEM base address slot, abort flag, two work-item slots
 
 // Bytes of one [128 x d] tile of `esize`-byte elements (Q, K and V tiles all
 // have this size since kBr == kBc): bf16 (esize 2) by default, E4M3 (esize 1)

@@ -116,21 +116,30 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
  * the combination step of the online softmax ("streaming reformulation" of the
  * IO-Aware Algorithms page) applied across segments.  The result is the same
  * operation as attn_fwd, up to floating-point rounding.
+ * Causal problems with more work units than SMs (units of unequal length) are
+ * not split; their persistent CTAs instead claim units dynamically, in the
+ * schedule's heaviest-first order, from a counter in `workspace` that this
+ * call zeroes on `stream` first.  Every unit is then computed exactly as by
+ * attn_fwd, so the outputs are bit-identical to attn_fwd's.
  *   arguments as attn_fwd, plus
  *   workspace       : device buffer of at least attn_fwd_split_workspace_bytes()
- *                     bytes, 16-byte aligned, owned by the caller; may be NULL
- *                     when that size is 0 (no split pays: this call then runs
- *                     exactly attn_fwd)
+ *                     bytes, 16-byte aligned, owned by the caller, not used by
+ *                     other work while this call runs; may be NULL when that
+ *                     size is 0 (this call then runs exactly attn_fwd)
  *   workspace_bytes : its size
- * Returns ATTN_ERR_INVALID_ARG when a split is chosen and the workspace is
- * missing, misaligned or too small; otherwise as attn_fwd.
+ * Returns ATTN_ERR_INVALID_ARG when a workspace is needed and it is missing,
+ * misaligned or too small; otherwise as attn_fwd.
  */
 int attn_fwd_split(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
                    int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace bytes attn_fwd_split needs on the current device; 0 when it would
- * not split (or the shape is invalid). */
+/* Workspace bytes attn_fwd_split needs on the current device; 0 when it needs
+ * none (or the shape is invalid). */
 size_t attn_fwd_split_workspace_bytes(int B, int H, int N, int d, int causal);
+
+/* K/V segments per split unit that attn_fwd_split chooses on the current
+ * device: 1 when it does not split, 0 for an invalid shape or no device. */
+int attn_fwd_split_segments(int B, int H, int N, int d, int causal);
 
 /*
  * attn_bwd - gradients of attn_fwd for an upstream gradient dO of O:

@@ -6,9 +6,13 @@ partial results of each row by their LSE weights.  The result is the same
 operation as attn_fwd, so the forward's tolerances apply unchanged: against the
 fp64 oracle max |dO| <= 2e-2 and per-row |dLSE| <= 1e-3 |LSE|.  The shapes below
 are chosen so that the launch splits units into 2, 3 and 4 segments on a
-152-SM GB300 (the test reads the split the library chose back from the
-workspace size and checks it is the expected one), with causal masks, ragged
-lengths, several schedule groups, and units left whole beside split ones.
+152-SM GB300 (the test checks the split the library reports is the expected
+one), with causal masks, ragged lengths, several schedule groups, and units
+left whole beside split ones.
+
+Causal problems with more units than SMs take the same entry's dynamic
+schedule instead: CTAs claim units from a counter in the workspace.  Each unit
+is computed as by attn_fwd, so those outputs must equal attn_fwd's bit for bit.
 """
 import pytest
 import torch
@@ -32,15 +36,8 @@ def built():
 
 
 def chosen_split(B, H, N, d, causal):
-    """Segments per split unit, recovered from the workspace size (1: no split)."""
-    need = ela.split_workspace_bytes(B, H, N, d, causal)
-    if need == 0:
-        return 1
-    rows = B * H * N
-    for s in range(2, 5):
-        if ((s * rows * d * 4 + 255) // 256) * 256 + s * rows * 4 == need:
-            return s
-    raise AssertionError(f"workspace size {need} matches no split factor")
+    """Segments per split unit that the library chose (1: no split)."""
+    return ela.split_segments(B, H, N, d, causal)
 
 
 # (B, H, N, d, causal, segments per split unit expected on 152 SMs).  Only the
@@ -96,10 +93,39 @@ def test_no_split_when_it_would_not_pay():
     """More units than SMs (the long-sequence workloads), or equal units that the idle SMs
     cannot all split: attn_fwd_split is attn_fwd."""
     needs_152_sms()
+    for shape in ((1, 16, 16384, 128, False), (1, 8, 65536, 128, True), (1, 8, 4096, 64, False),
+                  (1, 1, 256, 64, False)):
+        assert chosen_split(*shape) == 1
+    # non-causal: no workspace at all; causal with more units than SMs: the schedule counter only
     assert ela.split_workspace_bytes(1, 16, 16384, 128, False) == 0
-    assert ela.split_workspace_bytes(1, 8, 65536, 128, True) == 0
     assert ela.split_workspace_bytes(1, 8, 4096, 64, False) == 0
-    assert ela.split_workspace_bytes(1, 1, 256, 64, False) == 0
+    assert ela.split_workspace_bytes(1, 8, 65536, 128, True) == 256
+
+
+@pytest.mark.parametrize("B,H,N,d", [(2, 8, 8192, 64), (1, 5, 20000, 128), (3, 40, 1000, 64)])
+def test_dynamic_schedule_is_bit_identical(oracle_mod, B, H, N, d):
+    """Causal, more units than SMs: CTAs claim units dynamically; every unit is computed as by
+    the static schedule of attn_fwd, so O and LSE are equal bit for bit (and match the oracle)."""
+    needs_152_sms()
+    assert ela.split_workspace_bytes(B, H, N, d, True) == 256
+    q, k, v = workloads.make_inputs(B, H, N, d, seed=700 + N)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ws = torch.full((4096,), 0x5A, dtype=torch.uint8, device="cuda")
+    o, lse = ela.attn_fwd(qd, kd, vd, causal=True, workspace=ws[:256])
+    o_again, lse_again = ela.attn_fwd(qd, kd, vd, causal=True, workspace=ws[:256])
+    o1, lse1 = ela.attn_fwd(qd, kd, vd, causal=True, split=False)
+    torch.cuda.synchronize()
+    assert ela.last_device_error() == ela.ATTN_OK
+    assert torch.equal(o, o1) and torch.equal(lse, lse1)
+    assert torch.equal(o_again, o1) and torch.equal(lse_again, lse1)
+    assert (ws[256:] == 0x5A).all()  # nothing written past the counter block
+    rows = workloads.sample_rows(B * H, N, 6, seed=N)
+    O_ref, L_ref = oracle_mod.attention_rows(q, k, v, True, ela.default_scale(d), rows=rows.numpy())
+    idx = rows.cuda()
+    og = torch.gather(o.reshape(B * H, N, d), 1, idx[:, :, None].expand(-1, -1, d)).double().cpu().numpy()
+    lg = torch.gather(lse.reshape(B * H, N), 1, idx).double().cpu().numpy()
+    assert abs(og - O_ref).max() <= O_TOL
+    assert (abs(lg - L_ref) / abs(L_ref)).max() <= 1e-3
 
 
 def needs_152_sms():
