@@ -41,7 +41,7 @@ int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, con
     if (p.kv_split > 1) {
         // programmatic dependent launch: the combine kernel's CTAs may start as the
         // attention kernel's retire, and wait in-kernel for its completion
-        const size_t rows = static_cast<size_t>(p.BH) * p.N;
+        const int rows = p.split_units * 2 * kBr;  // the rows of the split units
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
         cfg.blockDim = dim3(256);
@@ -62,12 +62,15 @@ constexpr int kMaxUnitsForSplit = 1024;
 
 struct KvSplit {
     int segs;   // segments per split unit (1: no split)
-    int units;  // how many units, first in schedule order, are split
+    int units;  // how many units are split ...
+    int first;  // ... starting at this unit in schedule order
 };
 
 // Cost of the combine kernel, in K/V steps of one unit (measured: about 4 us
 // against about 1.2 us per K/V step of a query-tile pair).
 constexpr int kCombineSteps = 4;
+// Per-item cost besides its K/V steps (Q load, pipeline fill, epilogue), in K/V steps.
+constexpr int kItemSteps = 2;
 
 // The K/V split for a launch on num_sms SMs.  Only SMs that the units leave
 // idle take extra segments, so the launch stays one wave; the estimated time is
@@ -76,9 +79,33 @@ constexpr int kCombineSteps = 4;
 // (see decode_item).  The host walks the units in the kernel's schedule order
 // (decode_unit); a split is kept only when it shortens the estimate.
 KvSplit choose_kv_split(const attn_plan_t& plan, int num_sms, int BH, int N, int causal) {
-    KvSplit best{1, 0};
+    KvSplit best{1, 0, 0};
     const int units = plan.num_units;
-    if (units >= num_sms || units < 1) return best;
+    if (units < 1) return best;
+    if (units >= num_sms) {
+        // More units than SMs.  Causal units differ in length and take the
+        // dynamic schedule instead.  Non-causal units are equal: the static
+        // stride gives every CTA q = units / num_sms of them and R = units %
+        // num_sms CTAs one more, a last wave that leaves the other SMs idle.
+        // Splitting those R units into s segments spreads the last wave over
+        // all SMs: the first units - R items are whole (q per CTA), then come
+        // R * s segments in turn.
+        if (causal) return best;
+        const int L = (N + kBc - 1) / kBc;  // K/V steps of every unit
+        const int q = units / num_sms, R = units % num_sms;
+        if (R == 0) return best;
+        int best_cost = (q + 1) * (L + kItemSteps);
+        for (int s = 2; s <= kMaxKvSplit; ++s) {
+            if (s * (s - 1) >= L) break;
+            const int pieces_per_sm = (R * s + num_sms - 1) / num_sms;
+            const int cost = q * (L + kItemSteps) + pieces_per_sm * ((L + s - 1) / s + kItemSteps) + kCombineSteps;
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = KvSplit{s, R, units - R};
+            }
+        }
+        return best;
+    }
     const int nq = (N + kBr - 1) / kBr, nkv = (N + kBc - 1) / kBc, pairs = (nq + 1) / 2;
     const int G = plan.heads_per_group > 0 ? plan.heads_per_group : 1;
     int n0[kMaxUnitsForSplit], n1[kMaxUnitsForSplit];
@@ -114,7 +141,7 @@ KvSplit choose_kv_split(const attn_plan_t& plan, int num_sms, int BH, int N, int
         cost += kCombineSteps;
         if (cost < best_cost) {
             best_cost = cost;
-            best = KvSplit{s, U};
+            best = KvSplit{s, U, 0};
         }
     }
     return best;
@@ -130,15 +157,15 @@ bool use_dynamic_schedule(const attn_plan_t& plan, int num_sms, int causal) {
 // Workspace of attn_fwd_split: [256 B: the schedule counter][O partials][LSE partials].
 constexpr size_t kCounterBlock = 256;
 
-size_t split_part_o_bytes(int kv_split, int BH, int N, int d) {
-    const size_t b = static_cast<size_t>(kv_split) * BH * N * d * 4;
+size_t split_part_o_bytes(const KvSplit& s, int d) {
+    const size_t b = static_cast<size_t>(s.units) * s.segs * (2 * kBr) * d * 4;
     return (b + 255) & ~static_cast<size_t>(255);
 }
 
-size_t split_workspace_bytes(int kv_split, bool dynamic, int BH, int N, int d) {
-    if (kv_split <= 1 && !dynamic) return 0;
+size_t split_workspace_bytes(const KvSplit& s, bool dynamic, int d) {
+    if (s.segs <= 1 && !dynamic) return 0;
     size_t b = kCounterBlock;
-    if (kv_split > 1) b += split_part_o_bytes(kv_split, BH, N, d) + static_cast<size_t>(kv_split) * BH * N * 4;
+    if (s.segs > 1) b += split_part_o_bytes(s, d) + static_cast<size_t>(s.units) * s.segs * (2 * kBr) * 4;
     return b;
 }
 
@@ -152,10 +179,10 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     if ((st = attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan)) != ATTN_OK) return st;
 
     const int BH = B * H;
-    const KvSplit split = allow_split ? choose_kv_split(plan, dev->num_sms, BH, N, causal) : KvSplit{1, 0};
+    const KvSplit split = allow_split ? choose_kv_split(plan, dev->num_sms, BH, N, causal) : KvSplit{1, 0, 0};
     const int kv_split = split.segs;
     const bool dynamic = allow_split && use_dynamic_schedule(plan, dev->num_sms, causal);
-    const size_t need = split_workspace_bytes(kv_split, dynamic, BH, N, d);
+    const size_t need = split_workspace_bytes(split, dynamic, d);
     if (need > 0 && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need))
         return ATTN_ERR_INVALID_ARG;
     CUtensorMap tq, tk, tv;
@@ -177,12 +204,12 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     p.heads_per_group = plan.heads_per_group;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.kv_split = kv_split;
+    p.split_first = split.first;
     p.split_units = split.units;
-    p.num_items = split.units * kv_split + (plan.num_units - split.units);
+    p.num_items = plan.num_units + split.units * (kv_split - 1);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     p.part_o = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock) : nullptr;
-    p.part_lse = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + split_part_o_bytes(kv_split, BH, N, d))
-                              : nullptr;
+    p.part_lse = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + split_part_o_bytes(split, d)) : nullptr;
     p.sched_counter = dynamic ? reinterpret_cast<int*>(ws) : nullptr;
     if (dynamic) {
         cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), stream);
@@ -224,8 +251,8 @@ extern "C" size_t attn_fwd_split_workspace_bytes(int B, int H, int N, int d, int
     if (device_state(&dev) != ATTN_OK) return 0;
     attn_plan_t plan;
     if (attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan) != ATTN_OK) return 0;
-    return split_workspace_bytes(choose_kv_split(plan, dev->num_sms, B * H, N, causal).segs,
-                                 use_dynamic_schedule(plan, dev->num_sms, causal), B * H, N, d);
+    return split_workspace_bytes(choose_kv_split(plan, dev->num_sms, B * H, N, causal),
+                                 use_dynamic_schedule(plan, dev->num_sms, causal), d);
 }
 
 extern "C" int attn_fwd_split_segments(int B, int H, int N, int d, int causal) {
@@ -520,6 +547,7 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, voi
     p.heads_per_group = plan.heads_per_group;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.kv_split = 1;
+    p.split_first = 0;
     p.split_units = 0;
     p.num_items = plan.num_units;
     p.part_o = nullptr;

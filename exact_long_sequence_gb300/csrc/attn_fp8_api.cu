@@ -132,6 +132,7 @@ extern "C" int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void
     p.heads_per_group = plan.heads_per_group;
     p.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
     p.kv_split = 1;  // the FP8 kernel runs whole units
+    p.split_first = 0;
     p.split_units = 0;
     p.num_items = plan.num_units;
     p.part_o = nullptr;

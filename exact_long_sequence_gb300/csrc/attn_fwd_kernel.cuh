@@ -60,16 +60,18 @@ struct FwdParams {
     int heads_per_group;   // causal schedule only
     float scale_log2;      // scale * log2(e) (times the Q and K scales for the FP8 kernel)
     float out_scale;       // FP8 kernel: the V scale, applied with 1 / l; unused here
-    // K/V split (this kernel only; the FP8 kernel runs whole units): the first
-    // split_units units in schedule order are cut into kv_split segments of
-    // consecutive K/V tiles, one work item each; the other units are one item.
-    // A split item writes O / l and its LSE to part_o / part_lse, and
-    // attn_fwd_combine_kernel merges them.
+    // K/V split (this kernel only; the FP8 kernel runs whole units): the units
+    // [split_first, split_first + split_units) in schedule order are cut into
+    // kv_split segments of consecutive K/V tiles, one work item each; the other
+    // units are one item each, and the items follow unit order.  A split item
+    // writes O / l and its LSE to part_o / part_lse at its unit's ordinal among
+    // the split units, and attn_fwd_combine_kernel merges the segments.
     int kv_split;          // segments per split unit (1: no split)
+    int split_first;       // first split unit
     int split_units;       // units that are split (0: none)
-    int num_items;         // split_units * kv_split + (num_units - split_units)
-    float* part_o;         // [kv_split, BH, N, d] fp32
-    float* part_lse;       // [kv_split, BH, N] fp32 (natural log)
+    int num_items;         // num_units + split_units * (kv_split - 1)
+    float* part_o;         // [split_units, kv_split, 2 * kBr rows of the pair, d] fp32
+    float* part_lse;       // [split_units, kv_split, 2 * kBr] fp32 (natural log)
     // Dynamic work-item schedule (kernel instantiated with DYN): each CTA starts
     // with item blockIdx.x and then claims the next unclaimed item from this
     // counter (zero at launch), so items go out in schedule order to whichever
@@ -122,6 +124,7 @@ constexpr int kMaxKvSplit = 4;
 // least one key in every segment.
 struct ItemInfo {
     UnitInfo ui;
+    int u;       // unit index
     int seg;
     int nseg;
     int jb, je;
@@ -130,35 +133,30 @@ struct ItemInfo {
 template <bool CAUSAL>
 __device__ __forceinline__ ItemInfo decode_item(int w, const FwdParams& p) {
     ItemInfo it;
-    const int head_items = p.split_units * p.kv_split;
+    const int split_items = p.split_units * p.kv_split;
     int u;
-    if (w < head_items) {
-        u = w / p.kv_split;
-        it.seg = w - u * p.kv_split;
+    if (w < p.split_first) {  // whole units before the split range
+        u = w;
+        it.seg = 0;
+        it.nseg = 1;
+    } else if (w < p.split_first + split_items) {
+        const int r = w - p.split_first;
+        const int ord = r / p.kv_split;
+        u = p.split_first + ord;
+        it.seg = r - ord * p.kv_split;
         it.nseg = p.kv_split;
-    } else {
-        u = p.split_units + (w - head_items);
+    } else {  // whole units after it
+        u = w - split_items + p.split_units;
         it.seg = 0;
         it.nseg = 1;
     }
+    it.u = u;
     it.ui = decode_unit<CAUSAL>(u, p);
     const int n1 = it.ui.n[1];
     const int c = (n1 + it.nseg - 1) / it.nseg;
     it.jb = it.seg * c;
     it.je = min(n1, it.jb + c);
     return it;
-}
-
-// Inverse of decode_unit: the unit that holds query-tile pair `pair` of (batch,
-// head) bh.
-template <bool CAUSAL>
-__device__ __forceinline__ int unit_index(int bh, int pair, const FwdParams& p) {
-    if (!CAUSAL) return bh * p.num_pairs + pair;
-    const int G = p.heads_per_group;
-    const int g = bh / G;
-    const int heads_here = min(G, p.BH - g * G);
-    const int rank = p.num_pairs - 1 - pair;
-    return g * G * p.num_pairs + rank * heads_here + (bh - g * G);
 }
 
 // The producer hands each CTA's work items to the other roles through a ring of
@@ -607,7 +605,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (row_ok) p.LSE[grow_idx] = lse;
             } else {
                 // this segment's O / l (fp32) and LSE, merged later by the combine kernel
-                const size_t pidx = static_cast<size_t>(item.seg) * p.BH * p.N + grow_idx;
+                const size_t pidx = (static_cast<size_t>(item.u - p.split_first) * p.kv_split + item.seg) * (2 * kBr) +
+                                    t * kBr + rloc;
                 float4* orow = reinterpret_cast<float4*>(p.part_o + pidx * D);
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
@@ -646,27 +645,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 // results (O_s = softmax over the segment's keys times V, LSE_s),
 //     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
 // the same online-softmax combination as inside the kernel, across segments.
-// One warp per row; rows of unsplit units were written by the kernel itself.
+// One warp per row of the split units (2 kBr rows each); the rows of the other
+// units were written by the attention kernel itself.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(256) attn_fwd_combine_kernel(const FwdParams p) {
     constexpr int kPer = D / 32;  // columns per lane
     // launched as a programmatic dependent of the attention kernel: wait until
     // that grid has completed and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const size_t rows = static_cast<size_t>(p.BH) * p.N;
-    const size_t row = static_cast<size_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int prow = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);  // over split_units * 2 kBr
     const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const int bh = static_cast<int>(row / static_cast<size_t>(p.N));
-    const int i = static_cast<int>(row - static_cast<size_t>(bh) * p.N);
-    if (unit_index<CAUSAL>(bh, i / kBr / 2, p) >= p.split_units) return;
+    if (prow >= p.split_units * 2 * kBr) return;
+    const int ord = prow / (2 * kBr);
+    const int rr = prow - ord * 2 * kBr;  // row within the pair: tile rr / kBr, row rr % kBr
+    const UnitInfo ui = decode_unit<CAUSAL>(p.split_first + ord, p);
+    const int qrow = ui.q0 * kBr + rr;
+    if (qrow >= p.N) return;
+    const size_t row = static_cast<size_t>(ui.bh) * p.N + qrow;
     const int nseg = p.kv_split;
-    const size_t seg_stride = rows;
+    const size_t base = static_cast<size_t>(ord) * nseg * (2 * kBr) + rr;  // segment s at base + s * 2 kBr
     float lse[kMaxKvSplit];
     float mx = -INFINITY;
 #pragma unroll
     for (int s = 0; s < kMaxKvSplit; ++s) {
-        lse[s] = s < nseg ? p.part_lse[s * seg_stride + row] : -INFINITY;
+        lse[s] = s < nseg ? p.part_lse[base + s * (2 * kBr)] : -INFINITY;
         mx = fmaxf(mx, lse[s]);
     }
     float wsum = 0.f;
@@ -682,7 +684,7 @@ __global__ void __launch_bounds__(256) attn_fwd_combine_kernel(const FwdParams p
 #pragma unroll
     for (int s = 0; s < kMaxKvSplit; ++s) {
         if (s < nseg) {
-            const float* src = p.part_o + (s * seg_stride + row) * D + lane * kPer;
+            const float* src = p.part_o + (base + s * (2 * kBr)) * D + lane * kPer;
             const float ws = lse[s] * inv;
 #pragma unroll
             for (int c = 0; c < kPer; ++c) acc[c] = fmaf(ws, src[c], acc[c]);

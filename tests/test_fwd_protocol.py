@@ -12,8 +12,9 @@ arrival counts, ring depth and issue order, under many random interleavings.
 Where an arrival completes an asynchronous operation (a TMA load, an MMA
 commit), the model completes it at once, the most permissive timing for
 run-ahead.  It covers:
-  - whole units and the split segments of the K/V split (tile 0 visiting one
-    K/V tile fewer than tile 1 in causal units, several items per CTA);
+  - whole units and the split segments of the K/V split, for the heaviest units
+    and for the last units (tile 0 visiting one K/V tile fewer than tile 1 in
+    causal units, several items per CTA);
   - the static schedule and the dynamic one, in which the producer publishes
     each further item through a two-slot ring (ItemFull, 1 arrival; ItemEmpty,
     9 arrivals: the MMA warp and the eight softmax warps).
@@ -52,12 +53,12 @@ def unit_tiles(q0, nkv, causal):
     return [min(q0 + t + 1, nkv) if causal else nkv for t in (0, 1)]
 
 
-def items_of(units, nkv, causal, kv_split, split_units):
+def items_of(units, nkv, causal, kv_split, split_units, split_first=0):
     """(jb, je, n0) of every work item, in item order (the kernel's decode_item)."""
     out = []
     for u, q0 in enumerate(units):
         n = unit_tiles(q0, nkv, causal)
-        nseg = kv_split if u < split_units else 1
+        nseg = kv_split if split_first <= u < split_first + split_units else 1
         c = -(-n[1] // nseg)
         for s in range(nseg):
             jb = s * c
@@ -199,11 +200,11 @@ def run(items, seed, dynamic, stages=STAGES, empty_count=9, producer_waits_empty
     return None
 
 
-def cta_items(nq, causal, kv_split, split_units, pick):
+def cta_items(nq, causal, kv_split, split_units, pick, split_first=0):
     """The items of one CTA: `pick` selects which item indices it takes, in order."""
     pairs = (nq + 1) // 2
     units = [2 * (pairs - 1 - r) if causal else 2 * r for r in range(pairs)]  # heaviest first when causal
-    allitems = items_of(units, nq, causal, kv_split, split_units)
+    allitems = items_of(units, nq, causal, kv_split, split_units, split_first)
     return [allitems[i] for i in pick(len(allitems)) if i < len(allitems)]
 
 
@@ -216,6 +217,10 @@ CASES = [  # (query tiles, causal, kv_split, split units, CTA's item picks)
     (40, True, 1, 0, lambda n: [0, 5, 6, 11, 12, 19]),             # a dynamic claim order
     (3, True, 1, 0, lambda n: range(n)),                           # one K/V tile per item at the end
 ]
+TAIL_CASES = [  # the last units split (a partial last wave spread over all SMs)
+    (40, False, 4, 5, lambda n: range(0, n, 3), 15),
+    (33, False, 3, 2, lambda n: [0, 4] + list(range(15, n)), 15),
+]
 
 
 @pytest.mark.parametrize("dynamic", [False, True])
@@ -226,6 +231,15 @@ def test_protocol_has_no_overrun_and_no_deadlock(nq, causal, kv_split, split_uni
     for seed in range(25):
         assert run(items, seed, dynamic) is None
         assert run(items, seed, dynamic, stages=8) is None
+
+
+@pytest.mark.parametrize("dynamic", [False, True])
+@pytest.mark.parametrize("nq,causal,kv_split,split_units,pick,first", TAIL_CASES)
+def test_protocol_with_the_last_units_split(nq, causal, kv_split, split_units, pick, first, dynamic):
+    items = cta_items(nq, causal, kv_split, split_units, pick, first)
+    assert items
+    for seed in range(25):
+        assert run(items, seed, dynamic) is None
 
 
 def test_item_ring_cannot_run_ahead_even_without_its_empty_wait():

@@ -40,8 +40,9 @@ def chosen_split(B, H, N, d, causal):
     return ela.split_segments(B, H, N, d, causal)
 
 
-# (B, H, N, d, causal, segments per split unit expected on 152 SMs).  Only the
-# heaviest units, as many as the idle SMs allow, are split; the rest run whole.
+# (B, H, N, d, causal, segments per split unit expected on 152 SMs).  With fewer
+# units than SMs, the heaviest units are split, as many as the idle SMs allow.
+# With more (equal, non-causal) units, the units of the last partial wave are.
 CASES = [
     (1, 8, 4096, 64, True, 2),     # the causal d = 64 workload: 128 units, the 24 heaviest split
     (1, 2, 8192, 128, False, 2),   # 64 equal units, all split
@@ -50,6 +51,10 @@ CASES = [
     (2, 1, 2000, 128, True, 3),    # ragged causal, two batches in two schedule groups
     (1, 1, 4096, 128, False, 4),   # 16 units of 32 K/V tiles
     (1, 1, 8192, 64, True, 4),     # causal, 32 units of which 26 split
+    # more equal units than SMs: the last, partial wave's units are split
+    (1, 10, 4096, 128, False, 4),  # 160 units: 8 split into 4, spread over all SMs
+    (1, 13, 3000, 128, False, 4),  # 156 units, ragged length
+    (1, 16, 16384, 128, False, 4), # the long-sequence workload: 1024 units, the last 112 split
 ]
 
 
@@ -90,15 +95,16 @@ def test_split_parity(oracle_mod, B, H, N, d, causal, segs):
 
 
 def test_no_split_when_it_would_not_pay():
-    """More units than SMs (the long-sequence workloads), or equal units that the idle SMs
-    cannot all split: attn_fwd_split is attn_fwd."""
+    """Causal launches with more units than SMs, equal units that fill the SMs exactly or whose
+    last wave does not pay to split, or units the idle SMs cannot all split: no split."""
     needs_152_sms()
-    for shape in ((1, 16, 16384, 128, False), (1, 8, 65536, 128, True), (1, 8, 4096, 64, False),
-                  (1, 1, 256, 64, False)):
+    for shape in ((1, 8, 65536, 128, True), (1, 8, 4096, 64, False), (1, 1, 256, 64, False),
+                  (1, 19, 2048, 64, False), (2, 9, 4096, 64, False)):
         assert chosen_split(*shape) == 1
-    # non-causal: no workspace at all; causal with more units than SMs: the schedule counter only
-    assert ela.split_workspace_bytes(1, 16, 16384, 128, False) == 0
-    assert ela.split_workspace_bytes(1, 8, 4096, 64, False) == 0
+    # non-causal: no workspace at all (152 units fill the SMs exactly; 288 units: no split pays);
+    # causal with more units than SMs: the schedule counter only
+    assert ela.split_workspace_bytes(1, 19, 2048, 64, False) == 0
+    assert ela.split_workspace_bytes(2, 9, 4096, 64, False) == 0
     assert ela.split_workspace_bytes(1, 8, 65536, 128, True) == 256
 
 
