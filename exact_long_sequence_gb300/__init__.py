@@ -39,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "attn_fwd_split",
     "attn_fwd_split_workspace_bytes",
     "attn_fwd_split_segments",
+    "attn_fwd_split_choice",
     "attn_plan",
     "attn_last_device_error",
     "attn_last_cuda_error",
@@ -105,6 +106,9 @@ def load_library(path: str | None = None):
     lib.attn_fwd_split_workspace_bytes.restype = ctypes.c_size_t
     lib.attn_fwd_split_segments.argtypes = [i, i, i, i, i]
     lib.attn_fwd_split_segments.restype = i
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.attn_fwd_split_choice.argtypes = [i, i, i, i, i, i, ip, ip, ip, ip]
+    lib.attn_fwd_split_choice.restype = i
     lib.attn_plan.argtypes = [i, i, i, i, i, i, ctypes.POINTER(AttnPlan)]
     lib.attn_plan.restype = i
     lib.attn_last_device_error.argtypes = [vp]

@@ -255,6 +255,22 @@ extern "C" size_t attn_fwd_split_workspace_bytes(int B, int H, int N, int d, int
                                  use_dynamic_schedule(plan, dev->num_sms, causal), d);
 }
 
+extern "C" int attn_fwd_split_choice(int B, int H, int N, int d, int causal, int num_sms, int* segs,
+                                     int* first, int* units, int* dynamic) {
+    if (!segs || !first || !units || !dynamic || num_sms < 1) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || static_cast<long long>(B) * H * N >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    attn_plan_t plan;
+    const int st = attn_plan_impl(B, H, N, d, causal, num_sms, &plan);
+    if (st != ATTN_OK) return st;
+    const KvSplit s = choose_kv_split(plan, num_sms, B * H, N, causal);
+    *segs = s.segs;
+    *first = s.first;
+    *units = s.units;
+    *dynamic = use_dynamic_schedule(plan, num_sms, causal) ? 1 : 0;
+    return ATTN_OK;
+}
+
 extern "C" int attn_fwd_split_segments(int B, int H, int N, int d, int causal) {
     if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
     if (static_cast<long long>(B) * H * N >= (1ll << 31)) return 0;

@@ -142,6 +142,17 @@ size_t attn_fwd_split_workspace_bytes(int B, int H, int N, int d, int causal);
 int attn_fwd_split_segments(int B, int H, int N, int d, int causal);
 
 /*
+ * attn_fwd_split_choice - host only: the work split attn_fwd_split would use on
+ * a device with num_sms SMs.  Writes the segments per split unit (1: no split),
+ * the first split unit and the number of split units (in the kernel's unit
+ * order), and whether the dynamic schedule is used (0 or 1).  Returns
+ * ATTN_ERR_INVALID_ARG for a null pointer, num_sms < 1 or a shape out of range,
+ * ATTN_ERR_UNSUPPORTED for d other than 64 or 128.
+ */
+int attn_fwd_split_choice(int B, int H, int N, int d, int causal, int num_sms, int* segs, int* first, int* units,
+                          int* dynamic);
+
+/*
  * attn_bwd - gradients of attn_fwd for an upstream gradient dO of O:
  *     dV = P^T dO,  dS = P * (dO V^T - D) with D_i = sum_c dO_ic O_ic,
  *     dQ = scale * dS K,  dK = scale * dS^T Q,
