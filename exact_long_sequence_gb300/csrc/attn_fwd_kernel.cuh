@@ -20,6 +20,14 @@
 // abstract, here between TMA, the tensor core and the softmax warps):
 //     S0_j = Q0 K_j^T ; O1 += P1_{j-1} V_{j-1} ; S1_j = Q1 K_j^T ; O0 += P0_j V_j
 //
+// Work: a unit is a pair of query tiles of one (batch, head) against all the
+// K/V tiles they see.  A work item is a unit, or one segment of a unit's K/V
+// range when the launch is split (FwdParams::kv_split; a second kernel merges
+// the segments).  Persistent CTAs take items by a fixed stride, or claim them
+// from a counter when the kernel is instantiated with DYN (causal launches with
+// more units than SMs), the producer passing each claimed item to the other
+// roles through a two-slot shared-memory ring.
+//
 // TMEM columns: [0,128) S0 | [128,256) S1 | [256,256+d) O0 | [256+d,256+2d) O1.
 // P_t (bf16, two per column) is written over the first 64 columns of S_t once
 // the softmax has read S_t into registers.  The next S_t = Q_t K^T is issued
