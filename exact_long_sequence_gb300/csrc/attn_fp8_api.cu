@@ -57,12 +57,16 @@ __global__ void __launch_bounds__(256) transpose_v_e4m3(const uint8_t* V, uint8_
     }
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool DYN = false>
 int launch_fp8(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, const CUtensorMap& tk,
                const CUtensorMap& tvt, const FwdParams& p, cudaStream_t stream) {
-    auto kernel = attn_fwd_fp8_kernel<CAUSAL>;
+    if constexpr (CAUSAL && !DYN) {
+        // causal launches with a schedule counter take the dynamic instantiation
+        if (p.sched_counter != nullptr) return launch_fp8<CAUSAL, true>(dev, plan, tq, tk, tvt, p, stream);
+    }
+    auto kernel = attn_fwd_fp8_kernel<CAUSAL, DYN>;
     constexpr int smem = Fp8Layout::kSmem;
-    bool& configured = dev.fp8_smem_configured[CAUSAL];
+    bool& configured = dev.fp8_smem_configured[CAUSAL][DYN];
     cudaError_t e;
     if (!configured) {
         if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
@@ -81,9 +85,15 @@ bool positive_finite(float x) { return std::isfinite(x) && x > 0.f; }
 
 using namespace elsattn;
 
+// Workspace: the transposed V codes, then a 256-byte block for the schedule counter.
+size_t vt_bytes(int B, int H, int N, int d) {
+    const size_t b = static_cast<size_t>(B) * H * d * vt_pitch(N);
+    return (b + 255) & ~static_cast<size_t>(255);
+}
+
 extern "C" size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
-    return static_cast<size_t>(B) * H * d * vt_pitch(N);
+    return vt_bytes(B, H, N, d) + 256;
 }
 
 extern "C" int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void* O, float* LSE, int B, int H, int N,
@@ -139,6 +149,14 @@ extern "C" int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void
     p.part_lse = nullptr;
     p.sched_counter = nullptr;
     p.out_scale = v_scale;
+    // Causal units differ in length: with more of them than SMs, CTAs claim them
+    // dynamically (heaviest first) from a counter zeroed on the stream.
+    if (causal && plan.num_units > dev->num_sms) {
+        int* counter = reinterpret_cast<int*>(vt + vt_bytes(B, H, N, d));
+        cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+        p.sched_counter = counter;
+    }
     return causal ? launch_fp8<true>(*dev, plan, tq, tk, tvt, p, stream)
                   : launch_fp8<false>(*dev, plan, tq, tk, tvt, p, stream);
 }

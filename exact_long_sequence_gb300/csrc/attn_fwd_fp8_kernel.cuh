@@ -79,15 +79,23 @@ struct Fp8Layout {
     static constexpr int kOFull = kODone + 2;              // [2]
     static constexpr int kOEmpty = kOFull + 2;             // [2] (128)
     static constexpr int kDrain = kOEmpty + 2;             // [2] one per MMA warp
-    static constexpr int kNumBars = kDrain + 2;
-    static constexpr int kFlagsOff = kBarOff + kNumBars * 8;
+    static constexpr int kItemFull = kDrain + 2;           // [kItemRing] the slot holds the next unit index
+    static constexpr int kItemEmpty = kItemFull + kItemRing;  // [kItemRing] both MMA warps + 8 softmax warps read it
+    static constexpr int kNumBars = kItemEmpty + kItemRing;
+    static constexpr int kFlagsOff = kBarOff + kNumBars * 8;  // tmem base slot, abort flag, unit indices
+    static constexpr int kItemOff = kFlagsOff + 8;             // [kItemRing] int
     static constexpr int kBytes = kFlagsOff + 16;
     static constexpr int kSmem = kBytes + kSmemAlign;
     static_assert(kSmem <= kSmemLimit, "FP8 forward shared memory");
     static_assert(2 * kSmem > 233472, "one CTA per SM: it allocates all TMEM columns");
 };
 
-template <bool CAUSAL>
+// DYN: the dynamic unit schedule (p.sched_counter is set; causal launches with
+// more units than SMs): each CTA starts with unit blockIdx.x and then claims the
+// next unclaimed unit from the counter, the producer passing each claimed unit
+// to the MMA and softmax warps through a two-slot ring in shared memory (-1
+// after the last).  Without it, the static stride.
+template <bool CAUSAL, bool DYN = false>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_vt, const FwdParams p) {
@@ -127,6 +135,10 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         }
         mbar_init(bar(L::kDrain + 0), 1);
         mbar_init(bar(L::kDrain + 1), 1);
+        for (int s = 0; s < kItemRing; ++s) {
+            mbar_init(bar(L::kItemFull + s), 1);
+            mbar_init(bar(L::kItemEmpty + s), 10);
+        }
         fence_barrier_init();
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
@@ -140,6 +152,18 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kItemOff);
+    // Dynamic schedule, reader side (a whole warp calls it): ring entry r is this
+    // CTA's unit r + 1, or -1 after the last; false if the wait failed.
+    auto take_item = [&](uint32_t r, int& u) -> bool {
+        const uint32_t s = r % kItemRing;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(bar(L::kItemFull + s), (r / kItemRing) & 1u, ctx));
+        if (!got) return false;
+        u = item_slot[s];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::kItemEmpty + s));
+        return true;
+    };
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -149,7 +173,8 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         uint32_t ul = 0;
         uint32_t q_issued = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
+        uint32_t r = 0;  // dynamic schedule: ring entries published
+        for (int u = blockIdx.x; (DYN ? u >= 0 : u < p.num_units) && ok; ++ul) {
             const UnitInfo ui = decode_unit<CAUSAL>(u, p);
             q_issued = 0;
             for (int t = 0; t < 2 && ok; ++t) {
@@ -173,6 +198,20 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                     pos = pos.next(kFp8Stages);
                     ++issued;
                 }
+            }
+            if (!ok) break;
+            if constexpr (DYN) {
+                // claim this CTA's next unit and publish it to the other roles
+                u = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
+                if (u >= p.num_units) u = -1;
+                const uint32_t s = r % kItemRing;
+                if (r >= kItemRing && !(ok = mbar_wait(bar(L::kItemEmpty + s), ((r / kItemRing) - 1) & 1u, ctx)))
+                    break;
+                item_slot[s] = u;
+                mbar_arrive(bar(L::kItemFull + s));
+                ++r;
+            } else {
+                u += gridDim.x;
             }
         }
         if (!ok) {
@@ -210,7 +249,8 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
             const bool w = mbar_wait(b, parity, ctx);
             return __all_sync(0xffffffffu, w);
         };
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
+        uint32_t r = 0;
+        for (int u = blockIdx.x; (DYN ? u >= 0 : u < p.num_units) && ok; ++ul) {
             const UnitInfo ui = decode_unit<CAUSAL>(u, p);
             const int n1 = ui.n[1], nt = ui.n[t];
             ok = wait_all(bar(L::kQFull + t), ul & 1u);
@@ -283,6 +323,11 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                 vp = vp.next(kFp8Stages).next(kFp8Stages);
             }
             kpos = kp;
+            if constexpr (DYN) {
+                if (ok) ok = take_item(r++, u);
+            } else {
+                u += gridDim.x;
+            }
         }
         if (elect_one()) mma_commit(bar(L::kDrain + t));
         __syncwarp();
@@ -299,7 +344,8 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         uint32_t s_cnt = 0;  // S_t processed (all units)
         uint32_t ul = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++ul) {
+        uint32_t r = 0;
+        for (int u = blockIdx.x; (DYN ? u >= 0 : u < p.num_units) && ok; ++ul) {
             const UnitInfo ui = decode_unit<CAUSAL>(u, p);
             const int qt = ui.q0 + t;
             const int qrow = qt * kBr + rloc;
@@ -458,6 +504,11 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
             }
             tc_fence_before_sync();
             mbar_arrive(bar(L::kOEmpty + t));
+            if constexpr (DYN) {
+                ok = take_item(r++, u);
+            } else {
+                u += gridDim.x;
+            }
         }
     }
 

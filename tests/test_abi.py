@@ -157,7 +157,8 @@ def test_fp8_entry_validation(lib):
         assert lib.attn_fwd_fp8(*args, 128, 0, 0.125, *bad, *ws) == ela.ATTN_ERR_INVALID_ARG
     assert lib.attn_fwd_fp8(*args, 128, 0, 0.125, 1.0, 1.0, 1.0, None, 1 << 20, None) == ela.ATTN_ERR_INVALID_ARG
     assert lib.attn_fwd_fp8(*args, 128, 0, 0.125, 1.0, 1.0, 1.0, 0x6000, 16, None) == ela.ATTN_ERR_INVALID_ARG
-    assert lib.attn_fwd_fp8_workspace_bytes(2, 3, 100, 128) == 2 * 3 * 128 * 112
+    # the transposed V codes (rows padded to 16), 256-byte aligned, then the schedule counter block
+    assert lib.attn_fwd_fp8_workspace_bytes(2, 3, 100, 128) == (2 * 3 * 128 * 112 + 255) // 256 * 256 + 256
 
 
 def test_row_ops_validation(lib):

@@ -2,6 +2,10 @@
 
 The FP8 kernel (csrc/attn_fwd_fp8_kernel.cuh) has five roles: the TMA producer,
 one MMA-issuing warp per query tile and one softmax warpgroup per query tile.
+Causal launches with more units than SMs run a dynamic schedule: the producer
+publishes each further unit through a two-slot ring (ItemFull, 1 arrival;
+ItemEmpty, 10: both MMA warps and the eight softmax warps), which the model
+includes.
 They synchronise only through mbarriers, and an mbarrier wait names the phase
 it waits for by its parity alone.  The waiter of phase k therefore sees phase
 k + 2 as phase k.  The protocol must never let a barrier run two phases ahead
@@ -51,7 +55,7 @@ def unit_tiles(u, nq, BH, causal, heads_per_group):
     return [min(q0 + t + 1, nq) if causal else nq for t in (0, 1)]
 
 
-def run(units, nq, BH, causal, G, seed, per_buffer_p=True):
+def run(units, nq, BH, causal, G, seed, per_buffer_p=True, dynamic=False):
     """Returns None, or a description of a deadlock or of a phase overrun."""
     rng = random.Random(seed)
     B = {}
@@ -67,6 +71,8 @@ def run(units, nq, BH, causal, G, seed, per_buffer_p=True):
             mk((n, t))
         mk(("SCons", t), 128)
         mk(("OEmpty", t), 128)
+        mk(("ItemFull", t))           # dynamic schedule: the two ring slots
+        mk(("ItemEmpty", t), 10)      # both MMA warps and the eight softmax warps
         for b in (0, 1):
             mk(("PFree", t, b))
             mk(("PHalf", t, b), 128)
@@ -77,6 +83,9 @@ def run(units, nq, BH, causal, G, seed, per_buffer_p=True):
 
     def wait(name, phase):
         return name, phase
+
+    def take(r):  # reader side of the ring: entry r is the CTA's unit r + 1 (or the end)
+        yield wait(("ItemFull", r % 2), r // 2)
 
     def producer():
         pos = 0
@@ -92,6 +101,10 @@ def run(units, nq, BH, causal, G, seed, per_buffer_p=True):
                     yield wait(("KvEmpty", st), use - 1)
                 B[("KvFull", st)].arrive()
                 pos += 1
+            if dynamic:  # publish entry ul
+                if ul >= 2:
+                    yield wait(("ItemEmpty", ul % 2), ul // 2 - 1)
+                B[("ItemFull", ul % 2)].arrive()
 
     def mma(t):
         s_cnt = p_cnt = kpos = 0
@@ -129,6 +142,9 @@ def run(units, nq, BH, causal, G, seed, per_buffer_p=True):
                 B[("KvEmpty", vp % STAGES)].arrive()
                 vp += 2
             kpos = kp
+            if dynamic:
+                yield from take(ul)
+                B[("ItemEmpty", ul % 2)].arrive(1)
 
     def softmax(t):
         s = 0
@@ -146,6 +162,9 @@ def run(units, nq, BH, causal, G, seed, per_buffer_p=True):
                 s += 1
             yield wait(("OFull", t), ul)
             B[("OEmpty", t)].arrive(128)
+            if dynamic:
+                yield from take(ul)
+                B[("ItemEmpty", ul % 2)].arrive(4)
 
     roles = {"producer": producer(), "mma0": mma(0), "mma1": mma(1), "softmax0": softmax(0), "softmax1": softmax(1)}
     waiting = {k: None for k in roles}
@@ -181,13 +200,21 @@ CASES = [  # (query tiles per head, batch x heads, causal, grid, heads per group
 ]
 
 
+@pytest.mark.parametrize("dynamic", [False, True])
 @pytest.mark.parametrize("nq,BH,causal,grid,G", CASES)
-def test_protocol_has_no_overrun_and_no_deadlock(nq, BH, causal, grid, G):
+def test_protocol_has_no_overrun_and_no_deadlock(nq, BH, causal, grid, G, dynamic):
     units = BH * ((nq + 1) // 2)
     for block in range(0, min(grid, units), 5):
         mine = list(range(block, units, grid))[:3]
         for seed in range(12):
-            assert run(mine, nq, BH, causal, G, seed) is None
+            assert run(mine, nq, BH, causal, G, seed, dynamic=dynamic) is None
+
+
+def test_dynamic_schedule_with_a_claimed_unit_order():
+    """Units claimed out of stride order (as the counter hands them out), causal."""
+    for mine in ([0, 7, 9, 30, 31], [3, 4, 5], [60, 2, 13]):
+        for seed in range(20):
+            assert run(mine, 64, 8, True, 8, seed, dynamic=True) is None
 
 
 def test_checker_finds_the_single_p_barrier_race():
