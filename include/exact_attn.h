@@ -106,21 +106,25 @@ int attn_fwd_host(const void* Qh, const void* Kh, const void* Vh, void* Oh, floa
 size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
 
 /*
- * attn_fwd_split - attn_fwd that may also cut the K/V range of long units into
- * segments, for problems with fewer work units than SMs (few heads, or a
- * causal mask whose longest query tiles dominate).  Each segment is a work
- * item of its own; it writes its partial result (O over the segment's keys,
- * normalised, fp32, and that segment's LSE) to `workspace`, and a second
- * kernel on `stream` merges the segments of each row by
+ * attn_fwd_split - attn_fwd with a work schedule chosen for the launch's shape.
+ * A work unit is a pair of 128-row query tiles of one (batch, head) against
+ * every key they see.
+ *   - Fewer units than SMs (few heads, or a causal mask whose longest query
+ *     tiles dominate): the K/V range of the heaviest units is cut into
+ *     segments that run on the SMs the units leave idle.
+ *   - More equal units than SMs (no mask): the units of the last, partial wave
+ *     are cut into segments that spread over all SMs.
+ *   - More causal units than SMs (units of unequal length): no segments; the
+ *     persistent CTAs claim units dynamically, heaviest first, from a counter
+ *     in `workspace` that this call zeroes on `stream` first.  Every unit is
+ *     computed exactly as by attn_fwd, so the outputs are bit-identical to it.
+ * A segment is a work item of its own: it writes its partial result (O over
+ * the segment's keys, normalised, fp32, and that segment's LSE) to `workspace`,
+ * and a second kernel on `stream` merges the segments of each row by
  *     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
  * the combination step of the online softmax ("streaming reformulation" of the
  * IO-Aware Algorithms page) applied across segments.  The result is the same
  * operation as attn_fwd, up to floating-point rounding.
- * Causal problems with more work units than SMs (units of unequal length) are
- * not split; their persistent CTAs instead claim units dynamically, in the
- * schedule's heaviest-first order, from a counter in `workspace` that this
- * call zeroes on `stream` first.  Every unit is then computed exactly as by
- * attn_fwd, so the outputs are bit-identical to attn_fwd's.
  *   arguments as attn_fwd, plus
  *   workspace       : device buffer of at least attn_fwd_split_workspace_bytes()
  *                     bytes, 16-byte aligned, owned by the caller, not used by
