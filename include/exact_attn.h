@@ -249,22 +249,28 @@ int attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float
  * q_scale * e4m3(Q8) and likewise K, V.  Computes
  *     O = softmax(scale * Q K^T + mask) V   (bf16 [B,H,N,d]),  LSE (fp32 [B,H,N])
  * with S accumulated in fp32 from the exact code products, P rounded to E4M3
- * for the second product (four codes per TMEM column) and O / l in fp32.
+ * and staged in shared memory for the second product, and O / l in fp32.
+ * Causal launches with more work units than SMs run a dynamic schedule: CTAs
+ * claim units, heaviest first, from a counter in `workspace` that this call
+ * zeroes on `stream`; each unit is computed as under the static schedule.
  *   Q8, K8, V8 : const uint8 [B,H,N,d] E4M3 codes, device, 16-byte aligned
  *   O, LSE     : as attn_fwd
  *   q_scale, k_scale, v_scale : finite and > 0
  *   workspace  : device buffer of at least attn_fwd_fp8_workspace_bytes(), 16-byte
- *                aligned, owned by the caller: V transposed to [B,H,d,N] (rows
- *                padded to 16 bytes), written by this call
+ *                aligned, owned by the caller, not used by other work while this
+ *                call runs: V transposed to [B,H,d,N] (rows padded to 16 bytes),
+ *                then the schedule counter, written by this call
  * d must be 128 (ATTN_ERR_UNSUPPORTED otherwise).  Two launches on `stream`
- * (the transpose of V, then the attention kernel); the same argument, size and
- * error rules as attn_fwd otherwise.
+ * (the transpose of V, then the attention kernel; a 4-byte memset before the
+ * latter under the dynamic schedule); the same argument, size and error rules
+ * as attn_fwd otherwise.
  */
 int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void* O, float* LSE, int B, int H, int N, int d,
                  int causal, float scale, float q_scale, float k_scale, float v_scale, void* workspace,
                  size_t workspace_bytes, cudaStream_t stream);
 
-/* Device bytes attn_fwd_fp8 needs as workspace: B*H*d*ceil16(N); 0 for a non-positive size. */
+/* Device bytes attn_fwd_fp8 needs as workspace: B*H*d*ceil16(N) rounded up to 256,
+ * plus 256 for the schedule counter; 0 for a non-positive size. */
 size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
 
 /*
