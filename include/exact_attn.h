@@ -169,8 +169,9 @@ int attn_fwd_split_choice(int B, int H, int N, int d, int causal, int num_sms, i
  *   dQ, dK, dV     : bf16 [B,H,N,d] device pointers (written)
  *   workspace      : device buffer of at least attn_bwd_workspace_bytes() bytes,
  *                    16-byte aligned, owned by the caller: the fp32 dQ accumulator
- *                    [B,H,N,d], then D and LSE * log2(e) on rows padded to a
- *                    multiple of 128 per (batch, head)
+ *                    [B,H,N,d], then the row statistics -scale * D and
+ *                    -LSE * log2(e) (negated for the kernel's packed FMAs) on rows
+ *                    padded to a multiple of 128 per (batch, head)
  * Same size, alignment and error rules as attn_fwd; asynchronous on `stream`.
  */
 int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
