@@ -36,6 +36,11 @@ namespace elsattn {
 
 constexpr int kFp8Stages = 8;  // K/V ring depth (tiles of 16 KB)
 
+// P is stored as E4M3, whose largest finite value is 448 (2^8.81).  The
+// stale-max rule shared with the bf16 kernel keeps every term of P at most
+// 2^kRescaleLog2, so that bound must stay inside E4M3's range.
+static_assert(kRescaleLog2 <= 8.8f, "E4M3 P would saturate: the FP8 kernel needs its own threshold");
+
 // A bounded mbarrier wait without a function call, for the one wait that sits
 // where a row's 128 scores are live in registers (a call there forces them to
 // local memory).  Same semantics as mbar_wait.
