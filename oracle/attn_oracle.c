@@ -8,10 +8,9 @@
  * What it computes is the plain attention graph of "From Attention Graph to
  * FlashAttention - A Memory-Centric Compilation Approach in AICF", section 1
  * (Introduction): Scores = Q x K^T, Scores = Mask(Scores), Scores =
- * Softmax(Scores), Output = Scores x V.  The streaming pass that the CUDA path
- * runs is, per section 3 of the same page, a new execution structure for that
- * same operation, not a new operation, so its result must equal this one up to
- * rounding.  The AttenIO abstract ("I/O Analysis is All You Need", ASPLOS 2026)
+ * Softmax(Scores), Output = Scores x V.  Per section 3 of the same page, the
+ * streaming pass that the CUDA path runs changes only how that operation is
+ * executed, so its result must equal this one up to rounding.  The AttenIO abstract ("I/O Analysis is All You Need", ASPLOS 2026)
  * calls the target "exact" long-sequence self-attention for the same reason.
  *
  * Readings where the pages are silent (each one is also listed in the design
