@@ -16,8 +16,8 @@
 //
 // Two query tiles (Q0, Q1) share every K/V tile.  The MMA warp interleaves
 // them so that the tensor core works on one tile while the softmax of the
-// other runs ("fine-grained communication-computation overlap" in the AttenIO
-// abstract, here between TMA, the tensor core and the softmax warps):
+// other runs (the AttenIO abstract overlaps data movement with computation at
+// three levels; here the levels are TMA, the tensor core and the softmax warps):
 //     S0_j = Q0 K_j^T ; O1 += P1_{j-1} V_{j-1} ; S1_j = Q1 K_j^T ; O0 += P0_j V_j
 //
 // Work: a unit is a pair of query tiles of one (batch, head) against all the
