@@ -2,8 +2,9 @@
 
 Tolerance (a reading; the target states forward tolerances only): per gradient
 tensor, max |g_gpu - g_oracle| <= 2e-2 * max |g_oracle| + 1e-5. The kernel rounds P
-and dS to bf16 for the tensor core (relative 2^-9 each) and writes bf16 outputs
-(2^-9); 2e-2 of the tensor's largest entry leaves a wide margin over that. The
+and dS to bf16 for the tensor core (relative 2^-9 each), takes D from the bf16 O
+and writes bf16 outputs (2^-9). A CPU replay of that arithmetic
+(test_backward_model.py) reaches 0.15 to 0.30 of the bound. The
 absolute 1e-5 covers tensors that are exactly zero in exact arithmetic (with one
 key the softmax is constant, so dQ = dK = 0) where fp32 rounding of dP - D leaves
 ~1e-7 with the unit-scale inputs used here.
