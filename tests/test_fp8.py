@@ -11,7 +11,10 @@ value by at most 2^-4 of itself in the normal range and by at most 2^-10 below
 it, which gives, per element,
     |dO_ic| <= 2^-4 sum_j P_ij |v_jc| + 2^-10 sum_j |v_jc| / L_i + 2^-8 |O_ic| + 1e-6,
 the last two terms covering the bf16 output and the fp32 sums.  The bound is
-computed from the oracle's exact P.  A one-hot attention case (every query
+computed from the oracle's exact P.  On long peaked rows it is loose (its
+second term grows with the number of keys); test_fp8_model.py derives a
+per-term bound from the same rounding facts and checks the kernel's arithmetic
+against both on the CPU.  A one-hot attention case (every query
 attends to one key with weight 1, which E4M3 holds exactly) pins the layout of
 P and of the transposed V to the exact answer.
 """
