@@ -62,6 +62,12 @@ PINNED = {
     (1, 2, 8192, 128, False): (2, 0, 64, 0),     # 64 equal units, all split in two
     (1, 19, 2048, 64, False): (1, 0, 0, 0),      # 152 units fill the SMs exactly
     (1, 8, 4096, 64, False): (1, 0, 0, 0),       # 128 equal units: 24 spare SMs cannot halve them all
+    # the splits measured on a GB300 (GPU time per call, L2 flushed: unsplit -> split)
+    (1, 1, 1024, 64, False): (3, 0, 4, 0),       # 19.1 -> 16.0 us
+    (1, 1, 2048, 64, False): (4, 0, 8, 0),       # 27.3 -> 17.0 us
+    (1, 1, 4096, 64, False): (4, 0, 16, 0),      # 47.7 -> 23.2 us
+    (1, 1, 4096, 64, True): (3, 0, 13, 0),       # 47.8 -> 27.3 us
+    (1, 1, 8192, 64, True): (4, 0, 26, 0),       # 86.7 -> 35.5 us
 }
 
 
