@@ -3,9 +3,10 @@
 // back into TMEM -> tcgen05 O += P V -> O / l and LSE to global memory.
 //
 // The loop structure is the streaming schedule of "From Attention Graph to
-// FlashAttention - A Memory-Centric Compilation Approach in AICF", section 5
-// ("for q_tile: load Q_tile; for kv_tile: load K_tile, load V_tile, compute
-// score, update softmax, accumulate output"), mapped onto one GB300 SM:
+// FlashAttention - A Memory-Centric Compilation Approach in AICF", section 5:
+// each query tile is loaded once, and for every K/V tile the scores are
+// computed, the running softmax is updated and the output accumulated.  Here it
+// is mapped onto one GB300 SM:
 //
 //   warp 0 (one lane)   TMA producer: Q tiles once per unit, then K_j, V_j
 //                       into a ring of shared-memory stages.
@@ -34,13 +35,15 @@
 // after O_t += P_t V has been issued; tcgen05.mma operations of one thread run
 // in issue order on the SM's tensor core.
 //
-// Online softmax (the "streaming reformulation" of the IO-Aware Algorithms
+// Online softmax (the streaming reformulation of the IO-Aware Algorithms
 // page): per row, a reference maximum m (log2 units, scale folded in) and a
 // running sum l.  A tile whose row maximum exceeds m by more than
 // kRescaleLog2 moves m up and rescales l and the O accumulator by
 // 2^(m_old - m_new); smaller increases keep the stale m (the terms stay below
 // 2^kRescaleLog2 and the final O / l and LSE are unchanged by the choice of
-// m), which makes the O rescale rare after the first tiles.
+// m).  On N(0, 1) inputs no row moves m after its first tile; on inputs with
+// rare large entries (1 % of Q and K entries times 10) a warp still rescales
+// on about 40 % of its tiles.
 #pragma once
 
 #include <cuda.h>

@@ -122,8 +122,8 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
  * the segment's keys, normalised, fp32, and that segment's LSE) to `workspace`,
  * and a second kernel on `stream` merges the segments of each row by
  *     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
- * the combination step of the online softmax ("streaming reformulation" of the
- * IO-Aware Algorithms page) applied across segments.  The result is the same
+ * the combination step of the online softmax (the streaming reformulation of
+ * the IO-Aware Algorithms page) applied across segments.  The result is the same
  * operation as attn_fwd, up to floating-point rounding.
  *   arguments as attn_fwd, plus
  *   workspace       : device buffer of at least attn_fwd_split_workspace_bytes()
@@ -187,7 +187,7 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  * attn_plan - host only, launches nothing.  Fills *out with the tiling the
  * planner derives from an I/O count of the two tall-and-skinny products
  * (S = Q K^T and O = P V) against the shared- and tensor-memory capacity of an
- * sm_103 SM (the "I/O-optimal tiling" of the AttenIO abstract, "I/O Analysis
+ * sm_103 SM (the I/O-optimal tiling of the AttenIO abstract, "I/O Analysis
  * is All You Need", ASPLOS 2026).  num_sms <= 0 queries the current device.
  */
 int attn_plan(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out);
@@ -243,8 +243,8 @@ int attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float
 
 /*
  * attn_fwd_fp8 - the same forward on 8-bit inputs (the FP8 variant that the
- * NCG abstract's quantisation effects motivate, "Neural Computation Graph"
- * performance modelling: halved I/O and twice the tensor-core rate).  Q, K and V are given as
+ * quantisation effects of the Neural Circuit Graph (NCG) abstract's
+ * performance modelling motivate: halved I/O and twice the tensor-core rate).  Q, K and V are given as
  * E4M3 codes (OCP 8-bit floating point, E4M3: 1 sign, 4 exponent bits with
  * bias 7, 3 mantissa bits) with one fp32 scale per tensor; the real inputs are
  * q_scale * e4m3(Q8) and likewise K, V.  Computes
