@@ -8,10 +8,10 @@
  *     Output = Scores x V
  * with the scores multiplied by `scale`, plus the per-row log-sum-exp
  *     LSE_i = ln sum_j exp(scale * q_i . k_j)   (over the keys the mask keeps).
- * It is computed as the streaming pass of section 3 of that page ("load Q
- * tile, stream K/V tiles, compute partial scores, online softmax update,
- * accumulate output"): the N x N score and probability matrices never reach
- * device memory.  The library is the `flash_attention(Q, K, V)` call of
+ * It is computed as the streaming pass of section 3 of that page: a query
+ * tile stays on chip while the K/V tiles stream past it, each contributing its
+ * scores to a running softmax and to the output, so the N x N score and
+ * probability matrices never reach device memory.  The library is the `flash_attention(Q, K, V)` call of
  * section 4 of the same page, with the optional mask of section 5 as a flag.
  *
  * Conventions for every entry point:
