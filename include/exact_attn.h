@@ -3,10 +3,10 @@
  *
  * The operation is the attention graph of "From Attention Graph to
  * FlashAttention - A Memory-Centric Compilation Approach in AICF", section 1
- * (Introduction):
- *     Scores = Q x K^T ; Scores = Mask(Scores) ; Scores = Softmax(Scores) ;
- *     Output = Scores x V
- * with the scores multiplied by `scale`, plus the per-row log-sum-exp
+ * (Introduction): the query-key products, masked, normalised row by row with
+ * a softmax and applied to the values,
+ *     O = softmax(mask(scale * Q K^T)) V,
+ * plus the per-row log-sum-exp
  *     LSE_i = ln sum_j exp(scale * q_i . k_j)   (over the keys the mask keeps).
  * It is computed as the streaming pass of section 3 of that page: a query
  * tile stays on chip while the K/V tiles stream past it, each contributing its
