@@ -11,8 +11,9 @@
  * It is computed as the streaming pass of section 3 of that page: a query
  * tile stays on chip while the K/V tiles stream past it, each contributing its
  * scores to a running softmax and to the output, so the N x N score and
- * probability matrices never reach device memory.  The library is the `flash_attention(Q, K, V)` call of
- * section 4 of the same page, with the optional mask of section 5 as a flag.
+ * probability matrices never reach device memory.  The library is the
+ * `flash_attention(Q, K, V)` call of section 4 of the same page, with the
+ * optional mask of section 5 as a flag.
  *
  * Conventions for every entry point:
  *   - Q, K, V, O are bf16 tensors laid out [B, H, N, d], contiguous, d fastest;
