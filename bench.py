@@ -327,7 +327,7 @@ def run_gb300_fp8(args, w):
     import torch
 
     import exact_long_sequence_gb300 as ela
-    from exact_long_sequence_gb300 import _build
+    from exact_long_sequence_gb300 import _build, workloads
 
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
@@ -346,23 +346,11 @@ def run_gb300_fp8(args, w):
         dist.barrier()
     ela.load_library()
     stream = torch.cuda.current_stream(dev)
-    g = torch.Generator(device=dev).manual_seed(w.seed)
     shape = (w.B, w.H, w.N, w.d)
-    # Device-resident synthetic inputs with the workload's distributions, quantised per tensor to E4M3
-    # (scale = max|x| / 448).
-    xs = [torch.randn(shape, device=dev, generator=g) for _ in range(2)]
-    xs.append(torch.randn(shape, device=dev, generator=g) if w.v_dist == "normal"
-              else torch.rand(shape, device=dev, generator=g) * 2 - 1)
-    if w.qk_dist == "normal_spiky":
-        for i in range(2):
-            xs[i] = torch.where(torch.rand(shape, device=dev, generator=g) < 0.01, xs[i] * 10, xs[i])
-    codes, scales = [], []
-    for x in xs:
-        sc = float(x.abs().max()) / 448.0
-        codes.append((x / sc).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).contiguous())
-        scales.append(sc)
-    del xs
-    q8, k8, v8 = codes
+    # The workload's seeded draws quantised per tensor to E4M3 (scale = max|x| / 448) on the host,
+    # as the parity tests take them, then made resident in device memory.
+    q8, k8, v8, scales = workloads.make_inputs_fp8(w.B, w.H, w.N, w.d, w.seed, w.qk_dist, w.v_dist)
+    q8, k8, v8 = (t.to(dev) for t in (q8, k8, v8))
     o = torch.empty(shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
     ws = torch.empty(ela.load_library().attn_fwd_fp8_workspace_bytes(*shape), dtype=torch.uint8, device=dev)
@@ -561,7 +549,7 @@ def run_gb300_bwd(args, w):
     import torch
 
     import exact_long_sequence_gb300 as ela
-    from exact_long_sequence_gb300 import _build
+    from exact_long_sequence_gb300 import _build, workloads
 
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
@@ -578,9 +566,10 @@ def run_gb300_bwd(args, w):
         dist.barrier()
     ela.load_library()
     stream = torch.cuda.current_stream(dev)
-    g = torch.Generator(device=dev).manual_seed(w.seed)
     shape = (w.B, w.H, w.N, w.d)
-    q, k, v, do = (torch.randn(shape, device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
+    # seeded host draws of the workload's recipe (dO: the recipe's normal draw with seed + 1000)
+    q, k, v = (t.to(dev) for t in workloads.workload_inputs(w))
+    do = workloads.make_inputs(w.B, w.H, w.N, w.d, w.seed + 1000)[0].to(dev)
     o, lse = ela.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, stream=stream)
     ws = torch.empty(ela.load_library().attn_bwd_workspace_bytes(*shape), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -648,7 +637,7 @@ def run_gb300(args, w):
     import torch
 
     import exact_long_sequence_gb300 as ela
-    from exact_long_sequence_gb300 import _build
+    from exact_long_sequence_gb300 import _build, workloads
 
     rank, world, local = dist_env()
     if not torch.cuda.is_available():
@@ -666,26 +655,20 @@ def run_gb300(args, w):
     ela.load_library()
 
     stream = torch.cuda.current_stream(dev)
-    g = torch.Generator(device=dev).manual_seed(w.seed)
     shape = (w.B, w.H, w.N, w.d)
-    # Device-resident synthetic inputs with the workload's distributions (drawn on the GPU for speed).
-    q = torch.randn(shape, device=dev, generator=g)
-    k = torch.randn(shape, device=dev, generator=g)
-    v = torch.randn(shape, device=dev, generator=g) if w.v_dist == "normal" else torch.rand(shape, device=dev, generator=g) * 2 - 1
-    if w.qk_dist == "normal_spiky":
-        q = torch.where(torch.rand(shape, device=dev, generator=g) < 0.01, q * 10, q)
-        k = torch.where(torch.rand(shape, device=dev, generator=g) < 0.01, k * 10, k)
-    q, k, v = (t.to(torch.bfloat16).contiguous() for t in (q, k, v))
+    # The workload's seeded inputs, drawn on the host by the same recipe the parity tests check
+    # against the oracle, then made resident in device memory.
+    q, k, v = (t.to(dev) for t in workloads.workload_inputs(w))
     o = torch.empty_like(q)
     lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    # Workloads with fewer work units than SMs take the K/V split (attention kernel + combine
-    # kernel); its workspace is allocated once, outside the timed region.
-    # Causal workloads with more units than SMs take the dynamic schedule (a counter in the
-    # same workspace, zeroed by a memset on the stream before each launch).
+    # Workloads with fewer work units than SMs, or a partial last wave, take the K/V split (the
+    # segment that finishes a row last merges it in the kernel); causal workloads with more units
+    # than SMs take the dynamic schedule.  Both use a workspace allocated once, outside the timed
+    # region, whose counters a memset on the stream zeroes before each launch.
     split_bytes = ela.split_workspace_bytes(w.B, w.H, w.N, w.d, w.causal)
     split_ws = torch.empty(split_bytes, dtype=torch.uint8, device=dev) if split_bytes else None
-    launches_per_step = 2 if ela.split_segments(w.B, w.H, w.N, w.d, w.causal) > 1 else 1
+    launches_per_step = 1
 
     for _ in range(max(3, args.warmup)):
         ela.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream, workspace=split_ws)
@@ -758,9 +741,9 @@ def run_gb300(args, w):
                 "traffic": recorded_traffic(w.name),
                 "algorithmic_flops_per_launch": w.flops, "kernel_ms": kernel_ms,
                 "io_bound_bytes": w.io_bytes}
-    if launches_per_step == 2:
-        roofline["note"] = ("K/V split: the step is the attention kernel plus the combine kernel; "
-                            "the step time is used for both")
+    if split_bytes:
+        roofline["note"] = ("the step is the counters' memset and the attention kernel; "
+                            "the step time is used for the kernel")
     if peak_sustained:
         roofline["frac_of_sustained"] = achieved / peak_sustained
     line = {

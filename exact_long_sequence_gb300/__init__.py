@@ -45,7 +45,9 @@ EXPORTED_SYMBOLS = (
     "attn_last_cuda_error",
     "attn_strerror",
     "attn_debug_wait_timeout",
+    "attn_debug_arm_timeout",
     "attn_fwd_noalloc",
+    "attn_noalloc_last_device_error",
     "attn_bwd",
     "attn_bwd_workspace_bytes",
     "attn_fwd_fp8",
@@ -74,7 +76,7 @@ class AttnPlan(ctypes.Structure):
         ("num_units", ctypes.c_int), ("grid", ctypes.c_int), ("heads_per_group", ctypes.c_int),
         ("flops", ctypes.c_double), ("io_bytes", ctypes.c_double), ("l2_bytes", ctypes.c_double),
         ("hbm_bytes", ctypes.c_double), ("io_opt_q_tiles", ctypes.c_int), ("io_opt_Bc", ctypes.c_int),
-        ("io_opt_l2_bytes", ctypes.c_double),
+        ("io_opt_l2_bytes", ctypes.c_double), ("kv_in_flight_bytes", ctypes.c_double), ("l2_fit", ctypes.c_double),
     ]
 
     def as_dict(self):
@@ -119,8 +121,12 @@ def load_library(path: str | None = None):
     lib.attn_strerror.restype = ctypes.c_char_p
     lib.attn_debug_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.attn_debug_wait_timeout.restype = i
+    lib.attn_debug_arm_timeout.argtypes = [ctypes.c_uint64]
+    lib.attn_debug_arm_timeout.restype = i
     lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
     lib.attn_fwd_noalloc.restype = i
+    lib.attn_noalloc_last_device_error.argtypes = [vp]
+    lib.attn_noalloc_last_device_error.restype = i
     lib.attn_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, vp, ctypes.c_size_t, vp]
     lib.attn_bwd.restype = i
     lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
@@ -171,7 +177,7 @@ def split_segments(B: int, H: int, N: int, d: int, causal: bool) -> int:
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
-             split: bool = True, workspace=None):
+             split: bool = True, workspace=None, lib=None):
     """O, LSE = attention(q, k, v) on the GPU through the C ABI.
 
     q, k, v   : bf16 CUDA tensors [B, H, N, d], contiguous, d in {64, 128}
@@ -181,10 +187,12 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
                 and the dynamic schedule for causal problems with more (False: always attn_fwd)
     workspace : optional uint8 CUDA tensor of at least split_workspace_bytes() bytes for the
                 split (allocated here when needed and not given)
+    lib       : a library handle from load_library(path) (a compile-time variant); default: the
+                library built in-tree
     """
     import torch
 
-    lib = load_library()
+    lib = lib or load_library()
     if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
         raise ValueError("q, k, v must share a [B, H, N, d] shape")
     for t in (q, k, v):
@@ -251,13 +259,14 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
 
 
 def attn_fwd_fp8(q8, k8, v8, scales, causal: bool = False, scale: float | None = None, out=None, lse=None,
-                 workspace=None, stream=None):
+                 workspace=None, stream=None, lib=None):
     """FP8 forward: q8, k8, v8 are uint8 CUDA tensors [B, H, N, d] of E4M3 codes and
     `scales` = (q_scale, k_scale, v_scale), the real inputs being scale * e4m3(code).
-    Returns (o bf16 [B, H, N, d], lse fp32 [B, H, N]).  d must be 128."""
+    Returns (o bf16 [B, H, N, d], lse fp32 [B, H, N]).  d must be 128.  `lib`: a library handle
+    from load_library(path) (a compile-time variant); default: the library built in-tree."""
     import torch
 
-    lib = load_library()
+    lib = lib or load_library()
     for t in (q8, k8, v8):
         if t.shape != q8.shape or t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous():
             raise ValueError("q8, k8, v8 must be contiguous uint8 (E4M3 code) CUDA tensors of one [B, H, N, d] shape")
@@ -384,11 +393,22 @@ def attn_plan(B: int, H: int, N: int, d: int, causal: bool, num_sms: int = 0) ->
     return plan.as_dict()
 
 
-def last_device_error(stream=None) -> int:
+def last_device_error(stream=None, lib=None) -> int:
     """Synchronise `stream` and return (and clear) the kernel error status."""
-    return load_library().attn_last_device_error(_stream_handle(stream))
+    return (lib or load_library()).attn_last_device_error(_stream_handle(stream))
 
 
 def debug_wait_timeout(timeout_ns: int, stream=None) -> int:
     """Launch the bounded-wait test kernel (waits on a barrier nobody arrives on)."""
     return load_library().attn_debug_wait_timeout(int(timeout_ns), _stream_handle(stream))
+
+
+def debug_arm_timeout(timeout_ns: int) -> int:
+    """Arm the one-shot abort hook: the next forward launch runs with this wait limit and
+    withholds one of CTA 0's query-tile copies, so its wait runs out (test use only)."""
+    return load_library().attn_debug_arm_timeout(int(timeout_ns))
+
+
+def noalloc_last_device_error(stream=None) -> int:
+    """Synchronise `stream` and return (and clear) attn_fwd_noalloc's error status."""
+    return load_library().attn_noalloc_last_device_error(_stream_handle(stream))

@@ -27,17 +27,23 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every source to an object in parallel, then link the shared library."""
-    os.makedirs(LIB_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _deps_mtime():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, defines: dict | None = None, lib_path: str = LIB_PATH) -> str:
+    """Compile every source to an object in parallel, then link the shared library.
+
+    `defines` adds -D flags (compile-time variants of the kernels, e.g.
+    ELS_EXP2_POLY_PER32); such a variant is linked to `lib_path`, beside the
+    default library."""
+    os.makedirs(os.path.dirname(lib_path), exist_ok=True)
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= _deps_mtime():
+        return lib_path
     cc = nvcc()
     common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")] + ARCH
+    common += [f"-D{k}={v}" for k, v in sorted((defines or {}).items())]
     objs = []
+    tag = os.path.basename(lib_path)
 
     def compile_one(src):
-        obj = os.path.join(LIB_DIR, src + f".{os.getpid()}.o")
+        obj = os.path.join(LIB_DIR, src + f".{tag}.{os.getpid()}.o")
         cmd = [cc, "-c", os.path.join(CSRC, src), "-o", obj] + common
         if src.endswith(".cu") and verbose:
             cmd += ["-Xptxas", "-v"]
@@ -50,14 +56,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     r = subprocess.run([cc, "-shared", "-o", tmp] + objs + ARCH + ["-lcudart"], capture_output=True, text=True)
     for o in objs:
         os.remove(o)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build_variant(name: str, defines: dict, force: bool = False) -> str:
+    """A compile-time variant of the library, linked to _lib/libexact_attn_<name>.so."""
+    return build(force=force, defines=defines, lib_path=os.path.join(LIB_DIR, f"libexact_attn_{name}.so"))
 
 
 if __name__ == "__main__":

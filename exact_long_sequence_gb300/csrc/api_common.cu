@@ -112,7 +112,7 @@ int check_args(const void* Q, const void* K, const void* V, const void* O, const
     if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
     if (static_cast<long long>(B) * H * N >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
-    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return ATTN_ERR_MISALIGNED;
     if ((reinterpret_cast<uintptr_t>(LSE) & 3u) != 0) return ATTN_ERR_MISALIGNED;

@@ -5,10 +5,18 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <atomic>
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <functional>
+#include <map>
 #include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
 
 #include "../../include/exact_attn.h"
 #include "api_common.h"
@@ -19,6 +27,32 @@ extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sm
 
 namespace elsattn {
 namespace {
+
+// The scale's sign and size as the kernel takes them.  The kernel keeps a
+// running maximum of scale * s, so a negative scale runs as |scale| on the
+// negated scores (S = Q (-K)^T on the tensor core).  A zero scale (uniform
+// weights over the visible keys) runs with the smallest normal fp32 factor in
+// the exponents and 0 in the running maximum: every |factor * s| is then far
+// below 2^-24, so every exp2 term is exactly 1 in fp32, as it is for a zero
+// scale, masked scores still give 0, and LSE = ln(#visible) exactly.
+void set_scale(FwdParams& p, float scale) {
+    p.negate_scores = scale < 0.f ? 1u : 0u;
+    p.scale_log2 = scale == 0.f ? FLT_MIN : std::fabs(scale) * 1.4426950408889634f;
+    p.max_scale_log2 = scale == 0.f ? 0.f : p.scale_log2;
+}
+
+// Test hook (attn_debug_arm_timeout): a one-shot time limit for the next
+// forward launch, which also withholds CTA 0's first Q_0 copy; 0 = not armed.
+std::atomic<uint64_t> g_armed_timeout_ns{0};
+
+// Applies and disarms the hook, if armed.
+void take_armed_hook(FwdParams& p) {
+    const uint64_t t = g_armed_timeout_ns.exchange(0);
+    if (t != 0) {
+        p.timeout_ns = t;
+        p.withhold_first_q = 1u;
+    }
+}
 
 template <int D, bool CAUSAL, bool DYN = false>
 int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, const CUtensorMap& tk,
@@ -34,26 +68,11 @@ int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, con
         if (e != cudaSuccess) return cuda_fail(e);
         configured = true;
     }
-    const int grid = p.kv_split > 1 ? (p.num_items < dev.num_sms ? p.num_items : dev.num_sms) : plan.grid;
+    // every CTA starts with item blockIdx.x: the grid never exceeds the items
+    const int grid = p.num_items < dev.num_sms ? p.num_items : dev.num_sms;
     kernel<<<grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    if (p.kv_split > 1) {
-        // programmatic dependent launch: the combine kernel's CTAs may start as the
-        // attention kernel's retire, and wait in-kernel for its completion
-        const int rows = p.split_units * 2 * kBr;  // the rows of the split units
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
-        cfg.blockDim = dim3(256);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if ((e = cudaLaunchKernelEx(&cfg, attn_fwd_combine_kernel<D, CAUSAL>, p)) != cudaSuccess) return cuda_fail(e);
-    }
     return ATTN_OK;
 }
 
@@ -61,36 +80,63 @@ int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, con
 constexpr int kMaxUnitsForSplit = 1024;
 
 struct KvSplit {
-    int segs;   // segments per split unit (1: no split)
-    int units;  // how many units are split ...
-    int first;  // ... starting at this unit in schedule order
+    int segs;      // segments per split unit (1: no split)
+    int units;     // how many units are split ...
+    int first;     // ... starting at this unit in schedule order
+    bool dynamic;  // CTAs claim work items from a counter instead of a fixed stride
 };
 
-// Cost of the combine kernel, in K/V steps of one unit (measured: about 4 us
-// against about 1.2 us per K/V step of a query-tile pair).
-constexpr int kCombineSteps = 4;
-// Per-item cost besides its K/V steps (Q load, pipeline fill, epilogue), in K/V steps.
+// Per-item cost besides its K/V steps (Q load, pipeline fill, epilogue), in K/V
+// steps of a query-tile pair (one step measured at about 1.2 us).
 constexpr int kItemSteps = 2;
+// Extra cost of a segment: its partial result goes out in fp32, and the last
+// segment of each row reads the row's partials back and merges them.
+constexpr int kMergeSteps = 1;
 
-// The K/V split for a launch on num_sms SMs.  Only SMs that the units leave
-// idle take extra segments, so the launch stays one wave; the estimated time is
-// the longest work item in K/V steps (one step = one K/V tile for the pair),
-// plus the combine kernel.  A unit takes s segments only when s (s - 1) < n0
-// (see decode_item).  The host walks the units in the kernel's schedule order
-// (decode_unit); a split is kept only when it shortens the estimate.
-KvSplit choose_kv_split(const attn_plan_t& plan, int num_sms, int BH, int N, int causal) {
-    KvSplit best{1, 0, 0};
+// Greedy list scheduling of work items of the given costs (in order) on `grid`
+// CTAs: CTA i starts with item i, then every further item goes to the CTA that
+// becomes free first, as the dynamic schedule's counter hands them out.
+// Returns the time the last CTA finishes.
+int greedy_makespan(const int* cost, int items, int grid) {
+    std::priority_queue<int, std::vector<int>, std::greater<int>> free_at;
+    int i = 0;
+    for (; i < items && i < grid; ++i) free_at.push(cost[i]);
+    int end = 0;
+    for (; i < items; ++i) {
+        const int t = free_at.top();
+        free_at.pop();
+        free_at.push(t + cost[i]);
+    }
+    while (!free_at.empty()) {
+        end = free_at.top() > end ? free_at.top() : end;
+        free_at.pop();
+    }
+    return end;
+}
+
+// The work schedule of attn_fwd_split for a launch on num_sms SMs; one K/V
+// step is one K/V tile for a query-tile pair.
+//   - More causal units than SMs: the dynamic schedule, no split.
+//   - More non-causal (equal) units than SMs: the units of the last, partial
+//     wave are split so that their segments spread over all SMs.
+//   - Fewer units than SMs: the heaviest units (a prefix in the kernel's
+//     schedule order, decode_unit) are cut into s segments.  Either the split
+//     stays one wave on the SMs the units leave idle (static), or, for causal
+//     launches, any number of units are split and the CTAs claim the items
+//     dynamically, heaviest first (greedy_makespan estimates it).
+// A unit takes s segments only when s (s - 1) < n0 (see decode_item).  The
+// estimate with the least time wins; no split when none beats the unsplit one.
+KvSplit choose_kv_split_uncached(const attn_plan_t& plan, int num_sms, int BH, int N, int causal) {
+    KvSplit best{1, 0, 0, false};
     const int units = plan.num_units;
     if (units < 1) return best;
     if (units >= num_sms) {
-        // More units than SMs.  Causal units differ in length and take the
-        // dynamic schedule instead.  Non-causal units are equal: the static
-        // stride gives every CTA q = units / num_sms of them and R = units %
-        // num_sms CTAs one more, a last wave that leaves the other SMs idle.
-        // Splitting those R units into s segments spreads the last wave over
-        // all SMs: the first units - R items are whole (q per CTA), then come
-        // R * s segments in turn.
-        if (causal) return best;
+        if (causal) return KvSplit{1, 0, 0, units > num_sms};
+        // The static stride gives every CTA q = units / num_sms units and R =
+        // units % num_sms CTAs one more, a last wave that leaves the other SMs
+        // idle.  Splitting those R units into s segments spreads the last wave
+        // over all SMs: the first units - R items are whole (q per CTA), then
+        // come R * s segments in turn.
         const int L = (N + kBc - 1) / kBc;  // K/V steps of every unit
         const int q = units / num_sms, R = units % num_sms;
         if (R == 0) return best;
@@ -98,18 +144,18 @@ KvSplit choose_kv_split(const attn_plan_t& plan, int num_sms, int BH, int N, int
         for (int s = 2; s <= kMaxKvSplit; ++s) {
             if (s * (s - 1) >= L) break;
             const int pieces_per_sm = (R * s + num_sms - 1) / num_sms;
-            const int cost = q * (L + kItemSteps) + pieces_per_sm * ((L + s - 1) / s + kItemSteps) + kCombineSteps;
+            const int cost = q * (L + kItemSteps) + pieces_per_sm * ((L + s - 1) / s + kItemSteps + kMergeSteps);
             if (cost < best_cost) {
                 best_cost = cost;
-                best = KvSplit{s, R, units - R};
+                best = KvSplit{s, R, units - R, false};
             }
         }
         return best;
     }
+    if (units > kMaxUnitsForSplit) return best;
     const int nq = (N + kBr - 1) / kBr, nkv = (N + kBc - 1) / kBc, pairs = (nq + 1) / 2;
     const int G = plan.heads_per_group > 0 ? plan.heads_per_group : 1;
-    int n0[kMaxUnitsForSplit], n1[kMaxUnitsForSplit];
-    if (units > kMaxUnitsForSplit) return best;
+    std::vector<int> n0(units), n1(units);
     int longest = 0;
     for (int u = 0; u < units; ++u) {
         int pair;
@@ -125,47 +171,86 @@ KvSplit choose_kv_split(const attn_plan_t& plan, int num_sms, int BH, int N, int
         n1[u] = causal ? (q0 + 2 < nkv ? q0 + 2 : nkv) : nkv;
         if (n1[u] > longest) longest = n1[u];
     }
-    int best_cost = longest;
+    int best_cost = longest + kItemSteps;
+    std::vector<int> cost(units * kMaxKvSplit);
     for (int s = 2; s <= kMaxKvSplit; ++s) {
-        int U = (num_sms - units) / (s - 1);
-        if (U > units) U = units;
-        int k = 0;
-        while (k < U && s * (s - 1) < n0[k]) ++k;  // a prefix of units that can take s segments
-        U = k;
-        if (U == 0) continue;
-        int cost = 0;
-        for (int u = 0; u < units; ++u) {
-            const int steps = u < U ? (n1[u] + s - 1) / s : n1[u];
-            if (steps > cost) cost = steps;
+        int Umax = 0;  // the longest prefix of units that can take s segments
+        while (Umax < units && s * (s - 1) < n0[Umax]) ++Umax;
+        if (Umax == 0) continue;
+        // one wave: only the idle SMs take the extra segments
+        const int U1 = std::min(Umax, (num_sms - units) / (s - 1));
+        if (U1 > 0) {
+            int c = 0;
+            for (int u = 0; u < units; ++u) {
+                const int steps = u < U1 ? (n1[u] + s - 1) / s + kMergeSteps : n1[u];
+                c = std::max(c, steps + kItemSteps);
+            }
+            if (c < best_cost) {
+                best_cost = c;
+                best = KvSplit{s, U1, 0, false};
+            }
         }
-        cost += kCombineSteps;
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = KvSplit{s, U, 0};
+        if (!causal) continue;
+        // dynamic: every prefix length at which the split units' length changes
+        for (int U = 1; U <= Umax; ++U) {
+            if (U < Umax && n1[U] == n1[U - 1]) continue;
+            int items = 0;
+            for (int u = 0; u < units; ++u) {
+                if (u < U) {
+                    const int c = (n1[u] + s - 1) / s;
+                    for (int seg = 0; seg < s; ++seg) {
+                        const int jb = seg * c, je = std::min(n1[u], jb + c);
+                        cost[items++] = (je - jb) + kItemSteps + kMergeSteps;
+                    }
+                } else {
+                    cost[items++] = n1[u] + kItemSteps;
+                }
+            }
+            const int c = greedy_makespan(cost.data(), items, std::min(items, num_sms));
+            if (c < best_cost) {
+                best_cost = c;
+                best = KvSplit{s, U, 0, true};
+            }
         }
     }
     return best;
 }
 
-// Dynamic work-item schedule (FwdParams::sched_counter): for causal launches
-// with more units than SMs, whose units differ in length, so that a static
-// stride would leave some CTAs with more work than others.
-bool use_dynamic_schedule(const attn_plan_t& plan, int num_sms, int causal) {
-    return causal && plan.num_units > num_sms;
+// The choice for a shape is computed once and kept (the dynamic candidates
+// take a few hundred simulations of the item schedule).
+KvSplit choose_kv_split(const attn_plan_t& plan, int num_sms, int BH, int N, int causal) {
+    static std::mutex m;
+    static std::map<std::tuple<int, int, int, int, int, int>, KvSplit> cache;
+    const auto key = std::make_tuple(BH, N, plan.heads_per_group, plan.num_units, causal, num_sms);
+    {
+        std::lock_guard<std::mutex> lock(m);
+        const auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const KvSplit s = choose_kv_split_uncached(plan, num_sms, BH, N, causal);
+    std::lock_guard<std::mutex> lock(m);
+    if (cache.size() >= 4096) cache.clear();
+    cache.emplace(key, s);
+    return s;
 }
 
-// Workspace of attn_fwd_split: [256 B: the schedule counter][O partials][LSE partials].
+// Workspace of attn_fwd_split: [256 B: the schedule counter][per-row segment
+// counts of the split units][O partials][LSE partials], each part 256-aligned.
 constexpr size_t kCounterBlock = 256;
 
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+size_t split_count_bytes(const KvSplit& s) { return align256(static_cast<size_t>(s.units) * (2 * kBr) * 4); }
+
 size_t split_part_o_bytes(const KvSplit& s, int d) {
-    const size_t b = static_cast<size_t>(s.units) * s.segs * (2 * kBr) * d * 4;
-    return (b + 255) & ~static_cast<size_t>(255);
+    return align256(static_cast<size_t>(s.units) * s.segs * (2 * kBr) * d * 4);
 }
 
-size_t split_workspace_bytes(const KvSplit& s, bool dynamic, int d) {
-    if (s.segs <= 1 && !dynamic) return 0;
+size_t split_workspace_bytes(const KvSplit& s, int d) {
+    if (s.segs <= 1 && !s.dynamic) return 0;
     size_t b = kCounterBlock;
-    if (s.segs > 1) b += split_part_o_bytes(s, d) + static_cast<size_t>(s.units) * s.segs * (2 * kBr) * 4;
+    if (s.segs > 1)
+        b += split_count_bytes(s) + split_part_o_bytes(s, d) + static_cast<size_t>(s.units) * s.segs * (2 * kBr) * 4;
     return b;
 }
 
@@ -179,10 +264,10 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     if ((st = attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan)) != ATTN_OK) return st;
 
     const int BH = B * H;
-    const KvSplit split = allow_split ? choose_kv_split(plan, dev->num_sms, BH, N, causal) : KvSplit{1, 0, 0};
+    const KvSplit split = allow_split ? choose_kv_split(plan, dev->num_sms, BH, N, causal) : KvSplit{1, 0, 0, false};
     const int kv_split = split.segs;
-    const bool dynamic = allow_split && use_dynamic_schedule(plan, dev->num_sms, causal);
-    const size_t need = split_workspace_bytes(split, dynamic, d);
+    const bool dynamic = split.dynamic;
+    const size_t need = split_workspace_bytes(split, d);
     if (need > 0 && (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need))
         return ATTN_ERR_INVALID_ARG;
     CUtensorMap tq, tk, tv;
@@ -202,19 +287,24 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     p.num_pairs = (p.num_q_tiles + 1) / 2;
     p.num_units = plan.num_units;
     p.heads_per_group = plan.heads_per_group;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    set_scale(p, scale);
     p.kv_split = kv_split;
     p.split_first = split.first;
     p.split_units = split.units;
     p.num_items = plan.num_units + split.units * (kv_split - 1);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    p.part_o = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock) : nullptr;
-    p.part_lse = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + split_part_o_bytes(split, d)) : nullptr;
+    const size_t counts = kv_split > 1 ? split_count_bytes(split) : 0;
+    p.part_count = kv_split > 1 ? reinterpret_cast<int*>(ws + kCounterBlock) : nullptr;
+    p.part_o = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + counts) : nullptr;
+    p.part_lse =
+        kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + counts + split_part_o_bytes(split, d)) : nullptr;
     p.sched_counter = dynamic ? reinterpret_cast<int*>(ws) : nullptr;
-    if (dynamic) {
-        cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), stream);
+    if (dynamic || kv_split > 1) {
+        // the schedule counter and the per-row segment counts start at zero
+        cudaError_t e = cudaMemsetAsync(ws, 0, dynamic && kv_split == 1 ? sizeof(int) : kCounterBlock + counts, stream);
         if (e != cudaSuccess) return cuda_fail(e);
     }
+    take_armed_hook(p);
 
     if (d == 64)
         return causal ? launch<64, true>(*dev, plan, tq, tk, tv, p, stream)
@@ -251,8 +341,7 @@ extern "C" size_t attn_fwd_split_workspace_bytes(int B, int H, int N, int d, int
     if (device_state(&dev) != ATTN_OK) return 0;
     attn_plan_t plan;
     if (attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan) != ATTN_OK) return 0;
-    return split_workspace_bytes(choose_kv_split(plan, dev->num_sms, B * H, N, causal),
-                                 use_dynamic_schedule(plan, dev->num_sms, causal), d);
+    return split_workspace_bytes(choose_kv_split(plan, dev->num_sms, B * H, N, causal), d);
 }
 
 extern "C" int attn_fwd_split_choice(int B, int H, int N, int d, int causal, int num_sms, int* segs,
@@ -267,7 +356,7 @@ extern "C" int attn_fwd_split_choice(int B, int H, int N, int d, int causal, int
     *segs = s.segs;
     *first = s.first;
     *units = s.units;
-    *dynamic = use_dynamic_schedule(plan, num_sms, causal) ? 1 : 0;
+    *dynamic = s.dynamic ? 1 : 0;
     return ATTN_OK;
 }
 
@@ -418,7 +507,7 @@ extern "C" int attn_last_cuda_error(void) { return g_last_cuda_error; }
 extern "C" const char* attn_strerror(int status) {
     switch (status) {
         case ATTN_OK: return "success";
-        case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, size out of range, or scale not finite and > 0)";
+        case ATTN_ERR_INVALID_ARG: return "invalid argument (null pointer, size out of range, or a scale out of range)";
         case ATTN_ERR_UNSUPPORTED: return "unsupported (head dim must be 64 or 128; device must be sm_103)";
         case ATTN_ERR_MISALIGNED: return "misaligned pointer (tensors need 16-byte alignment, LSE 4-byte)";
         case ATTN_ERR_CUDA: return "CUDA call failed (see attn_last_cuda_error)";
@@ -455,6 +544,12 @@ extern "C" int attn_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t stream)
     wait_timeout_kernel<<<1, 32, 0, stream>>>(dev->error_word, timeout_ns);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+extern "C" int attn_debug_arm_timeout(uint64_t timeout_ns) {
+    if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return ATTN_ERR_INVALID_ARG;
+    g_armed_timeout_ns.store(timeout_ns);
+    return ATTN_OK;
 }
 
 // ----------------------------------------------------- allocation-free entry point
@@ -561,7 +656,7 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, voi
     p.num_pairs = (p.num_q_tiles + 1) / 2;
     p.num_units = plan.num_units;
     p.heads_per_group = plan.heads_per_group;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    set_scale(p, scale);
     p.kv_split = 1;
     p.split_first = 0;
     p.split_units = 0;
@@ -569,6 +664,7 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, voi
     p.part_o = nullptr;
     p.part_lse = nullptr;
     p.sched_counter = nullptr;
+    take_armed_hook(p);
 
     if (d == 64) {
         if (causal)
@@ -583,4 +679,20 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, voi
     }
     e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+extern "C" int attn_noalloc_last_device_error(cudaStream_t stream) {
+    NoAllocDevice* dev = nullptr;
+    int st = noalloc_device(&dev);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t word = 0;
+    if ((e = cudaMemcpyAsync(&word, dev->scratch, sizeof word, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(stream)) != cudaSuccess)
+        return cuda_fail(e);
+    if (word != 0 && ((e = cudaMemsetAsync(dev->scratch, 0, sizeof word, stream)) != cudaSuccess ||
+                      (e = cudaStreamSynchronize(stream)) != cudaSuccess))
+        return cuda_fail(e);
+    return word == kDevTimeout ? ATTN_ERR_TIMEOUT : (word == 0 ? ATTN_OK : ATTN_ERR_CUDA);
 }

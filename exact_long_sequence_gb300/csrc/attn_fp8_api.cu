@@ -101,7 +101,8 @@ extern "C" int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void
                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
     int st = check_args(Q8, K8, V8, O, LSE, B, H, N, d, scale);
     if (st != ATTN_OK) return st;
-    if (!positive_finite(q_scale) || !positive_finite(k_scale) || !positive_finite(v_scale))
+    // The FP8 kernel tracks the row maximum of the scaled scores assuming a positive factor.
+    if (!positive_finite(scale) || !positive_finite(q_scale) || !positive_finite(k_scale) || !positive_finite(v_scale))
         return ATTN_ERR_INVALID_ARG;
     if (d != kFp8D) return ATTN_ERR_UNSUPPORTED;
     if (!workspace) return ATTN_ERR_INVALID_ARG;

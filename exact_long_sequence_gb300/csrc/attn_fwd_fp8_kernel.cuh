@@ -36,6 +36,14 @@ namespace elsattn {
 
 constexpr int kFp8Stages = 8;  // K/V ring depth (tiles of 16 KB)
 
+// Scores out of every 32 of a row whose exp2 is evaluated on the FMA pipes
+// (exp2_poly.h) instead of the special-function unit: 0, 2, 4, ..., 16.
+#ifndef ELS_FP8_EXP2_POLY_PER32
+#define ELS_FP8_EXP2_POLY_PER32 0
+#endif
+constexpr int kFp8PolyPer32 = ELS_FP8_EXP2_POLY_PER32;
+static_assert(kFp8PolyPer32 >= 0 && kFp8PolyPer32 <= 16 && kFp8PolyPer32 % 2 == 0, "FP8 exp2 offload: even, <= 16");
+
 // P is stored as E4M3, whose largest finite value is 448 (2^8.81).  The
 // stale-max rule shared with the bf16 kernel keeps every term of P at most
 // 2^kRescaleLog2, so that bound must stay inside E4M3's range.
@@ -176,12 +184,14 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         RingPos pos{0u, 0u};
         uint32_t issued = 0;
         uint32_t ul = 0;
-        uint32_t q_issued = 0;
+        uint32_t q_issued = 0;  // bit t: a Q_t load of the latest unit was issued ...
+        uint32_t q_parity = 0;  // ... and completes this phase parity of QFull[t]
         bool ok = true;
         uint32_t r = 0;  // dynamic schedule: ring entries published
         for (int u = blockIdx.x; (DYN ? u >= 0 : u < p.num_units) && ok; ++ul) {
             const UnitInfo ui = decode_unit<CAUSAL>(u, p);
             q_issued = 0;
+            q_parity = ul & 1u;
             for (int t = 0; t < 2 && ok; ++t) {
                 ok = mbar_wait(bar(L::kQEmpty + t), (ul & 1u) ^ 1u, ctx);
                 if (!ok) break;
@@ -219,16 +229,17 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                 u += gridDim.x;
             }
         }
-        if (!ok) {
-            const uint32_t pending = issued < static_cast<uint32_t>(kFp8Stages) ? issued : kFp8Stages;
-            RingPos back = pos;
-            for (uint32_t i = 0; i < pending; ++i) {
-                back = back.stage == 0 ? RingPos{kFp8Stages - 1u, back.phase ^ 1u} : RingPos{back.stage - 1, back.phase};
-                mbar_wait_drain(bar(L::kKvFull + back.stage), back.phase, 50000000ull);
-            }
-            for (int t = 0; t < 2; ++t)
-                if (q_issued & (1u << t)) mbar_wait_drain(bar(L::kQFull + t), ul & 1u, 50000000ull);
+        // Every issued copy lands before the CTA's shared memory is released
+        // (bounded waits; they return at once after a normal run, whose phases
+        // have all completed, and matter after an abort by any role).
+        const uint32_t pending = issued < static_cast<uint32_t>(kFp8Stages) ? issued : kFp8Stages;
+        RingPos back = pos;
+        for (uint32_t i = 0; i < pending; ++i) {
+            back = back.stage == 0 ? RingPos{kFp8Stages - 1u, back.phase ^ 1u} : RingPos{back.stage - 1, back.phase};
+            mbar_wait_drain(bar(L::kKvFull + back.stage), back.phase, 50000000ull);
         }
+        for (int t = 0; t < 2; ++t)
+            if (q_issued & (1u << t)) mbar_wait_drain(bar(L::kQFull + t), q_parity, 50000000ull);
     } else if (warp == 1 || warp == 2) {
         // ------------------------------------------------------------ MMA issuers
         // Warp 1 issues tile 0's products, warp 2 tile 1's: with P in shared memory
@@ -433,10 +444,20 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                         float x0, x1, x2, x3;  // exponents, two per packed instruction
                         ffma2(x0, x1, sc[2 * c], sc[2 * c + 1], sl2, -m_use);
                         ffma2(x2, x3, sc[2 * c + 2], sc[2 * c + 3], sl2, -m_use);
-                        const float a0 = ex2_approx(x0);
-                        const float b0 = ex2_approx(x1);
-                        const float a1 = ex2_approx(x2);
-                        const float b1 = ex2_approx(x3);
+                        float a0, b0, a1, b1;
+                        // the first kFp8PolyPer32 scores of every 32 on the FMA pipes
+                        if (2 * c < kFp8PolyPer32) {
+                            exp2_poly2(a0, b0, x0, x1);
+                        } else {
+                            a0 = ex2_approx(x0);
+                            b0 = ex2_approx(x1);
+                        }
+                        if (2 * c + 2 < kFp8PolyPer32) {
+                            exp2_poly2(a1, b1, x2, x3);
+                        } else {
+                            a1 = ex2_approx(x2);
+                            b1 = ex2_approx(x3);
+                        }
                         fadd2(acc0, acc1, a0, b0);
                         fadd2(acc2, acc3, a1, b1);
                         pk[c / 2] = pack_e4m3x4(a0, b0, a1, b1);

@@ -23,11 +23,12 @@
 //
 // Work: a unit is a pair of query tiles of one (batch, head) against all the
 // K/V tiles they see.  A work item is a unit, or one segment of a unit's K/V
-// range when the launch is split (FwdParams::kv_split; a second kernel merges
-// the segments).  Persistent CTAs take items by a fixed stride, or claim them
-// from a counter when the kernel is instantiated with DYN (causal launches with
-// more units than SMs), the producer passing each claimed item to the other
-// roles through a two-slot shared-memory ring.
+// range when the launch is split (FwdParams::kv_split; the segment that
+// finishes a row last merges the row's segments).  Persistent CTAs take items
+// by a fixed stride, or claim them from a counter when the kernel is
+// instantiated with DYN (launches whose items differ in length), the producer
+// passing each claimed item to the other roles through a two-slot
+// shared-memory ring.
 //
 // TMEM columns: [0,128) S0 | [128,256) S1 | [256,256+d) O0 | [256+d,256+2d) O1.
 // P_t (bf16, two per column) is written over the first 64 columns of S_t once
@@ -49,12 +50,31 @@
 #include <cuda.h>
 #include <cstdint>
 
+#include "exp2_poly.h"
 #include "plan.h"
 #include "sm103_ptx.cuh"
 
+// Scores out of every 32 of a row whose exp2 is evaluated on the FMA pipes
+// (exp2_poly.h) instead of the special-function unit: 0, 2, 4, 6 or 8.
+#ifndef ELS_EXP2_POLY_PER32
+#define ELS_EXP2_POLY_PER32 0
+#endif
+// Stale-maximum threshold of this kernel, log2 units (see kRescaleLog2Bf16).
+#ifndef ELS_RESCALE_LOG2_BF16
+#define ELS_RESCALE_LOG2_BF16 8
+#endif
+
 namespace elsattn {
 
+// Threshold of the FP8 kernel, whose P is E4M3 (at most 448): terms must stay
+// at most 2^8.
 constexpr float kRescaleLog2 = 8.0f;
+// Threshold of the bf16 kernel: terms stay at most 2^T, so l <= N 2^T and
+// |O_acc| <= N 2^T max|V| in fp32.
+constexpr float kRescaleLog2Bf16 = ELS_RESCALE_LOG2_BF16;
+static_assert(kRescaleLog2Bf16 >= 1.0f && kRescaleLog2Bf16 <= 64.0f, "stale-maximum threshold out of range");
+constexpr int kPolyPer32 = ELS_EXP2_POLY_PER32;
+static_assert(kPolyPer32 >= 0 && kPolyPer32 <= 8 && kPolyPer32 % 2 == 0, "exp2 offload: 0, 2, 4, 6 or 8 per 32");
 constexpr float kLn2 = 0.693147180559945309f;
 
 struct FwdParams {
@@ -76,19 +96,34 @@ struct FwdParams {
     // kv_split segments of consecutive K/V tiles, one work item each; the other
     // units are one item each, and the items follow unit order.  A split item
     // writes O / l and its LSE to part_o / part_lse at its unit's ordinal among
-    // the split units, and attn_fwd_combine_kernel merges the segments.
+    // the split units and counts itself in part_count; the segment that counts
+    // a row last merges that row's segments (merge_split_row).
     int kv_split;          // segments per split unit (1: no split)
     int split_first;       // first split unit
     int split_units;       // units that are split (0: none)
     int num_items;         // num_units + split_units * (kv_split - 1)
     float* part_o;         // [split_units, kv_split, 2 * kBr rows of the pair, d] fp32
     float* part_lse;       // [split_units, kv_split, 2 * kBr] fp32 (natural log)
+    int* part_count = nullptr;  // [split_units, 2 * kBr]: segments of the row written so far (zero at launch)
     // Dynamic work-item schedule (kernel instantiated with DYN): each CTA starts
     // with item blockIdx.x and then claims the next unclaimed item from this
     // counter (zero at launch), so items go out in schedule order to whichever
     // CTA is free first.  Static schedule (nullptr): CTA b takes items b,
     // b + grid, b + 2 grid, ...
     int* sched_counter;
+    // Nonzero: S = Q (-K)^T (the instruction descriptor's negate-B bit).  A
+    // negative scale is run as |scale| on the negated scores, so the kernel's
+    // running maximum always tracks the largest scaled score.  (bf16 kernel only.)
+    uint32_t negate_scores = 0;
+    // Factor of a tile's raw score maximum in the running maximum: scale_log2,
+    // except 0 for a zero scale, whose scale_log2 is the smallest normal float
+    // (every term is then exactly 1 and the running maximum stays exactly 0,
+    // so LSE = ln(#visible keys) exactly).  (bf16 kernel only.)
+    float max_scale_log2 = 0.f;
+    // Test hook: nonzero makes CTA 0 arm the barrier of its first Q_0 load
+    // without issuing the copy, so that a wait on it runs out of time and the
+    // kernel takes its abort path.  Zero in every normal launch.
+    uint32_t withhold_first_q = 0;
 };
 
 struct UnitInfo {
@@ -212,6 +247,68 @@ struct SmemLayout {
     static_assert(kBytes + kSmemAlign <= smem_bytes_for(D), "shared memory layout exceeds the plan");
 };
 
+// Merge the segments of one row of a split unit: with the segments' partial
+// results (O_s = softmax over the segment's keys times V, and LSE_s),
+//     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
+// the same online-softmax combination the kernel applies across K/V tiles,
+// here across segments.  Run by the thread of the segment that finished the
+// row last, after every segment's row is visible; it writes O (bf16) and LSE,
+// then discards the row's partial O lines from L2 (nothing reads them again,
+// so they need not be written back to device memory).  Segment s of the row
+// is at part_o / part_lse index base + s 2 kBr.
+template <int D>
+__device__ __forceinline__ void merge_split_row(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                                             __nv_bfloat16* O, float* LSE, size_t base, int nseg, size_t out_row) {
+    float w[kMaxKvSplit];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) {
+        w[s] = s < nseg ? __ldcg(part_lse + base + s * (2 * kBr)) : -INFINITY;
+        mx = fmaxf(mx, w[s]);
+    }
+    float wsum = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) {
+        w[s] = s < nseg ? expf(w[s] - mx) : 0.f;
+        wsum += w[s];
+    }
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) w[s] *= inv;
+    uint4* dst = reinterpret_cast<uint4*>(O + out_row * D);
+#pragma unroll 2
+    for (int c = 0; c < D; c += 8) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < kMaxKvSplit; ++s) {
+            if (s < nseg) {
+                const float4* src = reinterpret_cast<const float4*>(part_o + (base + s * (2 * kBr)) * D + c);
+                const float4 a = __ldcg(src), b = __ldcg(src + 1);
+                acc[0] = fmaf(w[s], a.x, acc[0]);
+                acc[1] = fmaf(w[s], a.y, acc[1]);
+                acc[2] = fmaf(w[s], a.z, acc[2]);
+                acc[3] = fmaf(w[s], a.w, acc[3]);
+                acc[4] = fmaf(w[s], b.x, acc[4]);
+                acc[5] = fmaf(w[s], b.y, acc[5]);
+                acc[6] = fmaf(w[s], b.z, acc[6]);
+                acc[7] = fmaf(w[s], b.w, acc[7]);
+            }
+        }
+        dst[c / 8] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                                pack_bf16x2(acc[6], acc[7]));
+    }
+    LSE[out_row] = mx + logf(wsum);
+    // every value read above has been consumed by the stores: drop the lines
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) {
+        if (s < nseg) {
+            const float* row = part_o + (base + s * (2 * kBr)) * D;
+#pragma unroll
+            for (int b = 0; b < D * 4; b += 128) l2_discard_line(reinterpret_cast<const char*>(row) + b);
+        }
+    }
+}
+
 // DYN: the dynamic work-item schedule (p.sched_counter is set); without it the
 // static schedule is compiled with no trace of the item ring.
 template <int D, bool CAUSAL, bool DYN = false>
@@ -264,10 +361,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    // A split launch's combine kernel may be scheduled onto SMs as this grid's
-    // CTAs retire; it waits for this whole grid (griddepcontrol.wait) before it
-    // reads the partial results.
-    if (p.kv_split > 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kItemOff);
     // Every role starts with item blockIdx.x (the grid never exceeds the item
     // count).  The static schedule then advances by gridDim.x; the dynamic one
@@ -288,11 +381,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         RingPos pos{0u, 0u};      // next ring position to fill
         uint32_t issued = 0;      // ring fills issued so far
         uint32_t ul = 0;
-        uint32_t q_issued = 0;    // bit t: a Q_t load of local unit (ul) is in flight
+        uint32_t q_issued = 0;    // bit t: a Q_t load of the latest item was issued ...
+        uint32_t q_parity = 0;    // ... and completes this phase parity of QFull[t]
         bool ok = true;
         uint32_t r = 0;  // dynamic schedule: ring entries published
         for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok;) {
             q_issued = 0;
+            q_parity = ul & 1u;
             const ItemInfo item = decode_item<CAUSAL>(w, p);
             const UnitInfo& ui = item.ui;
             for (int t = 0; t < 2 && ok; ++t) {
@@ -300,9 +395,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(L::kQFull + t), L::kTile);
                 const uint32_t dst = s_base + L::kQOff + t * L::kTile;
+                if (!(p.withhold_first_q && blockIdx.x == 0 && ul == 0 && t == 0)) {
 #pragma unroll
-                for (int b = 0; b < D / 64; ++b)
-                    tma_load_3d(dst + b * (kBr * 128), &tmap_q, bar(L::kQFull + t), b * 64, (ui.q0 + t) * kBr, ui.bh);
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_load_3d(dst + b * (kBr * 128), &tmap_q, bar(L::kQFull + t), b * 64, (ui.q0 + t) * kBr, ui.bh);
+                }
                 q_issued |= 1u << t;
             }
             for (int j = item.jb; j < item.je && ok; ++j) {
@@ -336,25 +433,25 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 w += gridDim.x;
             }
         }
-        if (!ok) {
-            // Abort: wait (bounded) for the copies still in flight before the
-            // CTA's shared memory is released.  The last min(issued, stages)
-            // fills are the only ones that can still be pending.
-            const uint32_t pending = issued < static_cast<uint32_t>(L::kStages) ? issued : L::kStages;
-            RingPos back = pos;
-            for (uint32_t i = 0; i < pending; ++i) {
-                back = back.stage == 0 ? RingPos{L::kStages - 1u, back.phase ^ 1u} : RingPos{back.stage - 1, back.phase};
-                mbar_wait_drain(bar(L::kKvFull + back.stage), back.phase, 50000000ull);
-            }
-            for (int t = 0; t < 2; ++t)
-                if (q_issued & (1u << t)) mbar_wait_drain(bar(L::kQFull + t), ul & 1u, 50000000ull);
+        // Every issued copy lands before the CTA's shared memory is released
+        // (bounded waits).  Only the last min(issued, stages) fills and the
+        // latest item's Q loads can still be pending: after a normal run their
+        // phases have completed and these waits return at once; after an abort
+        // (this role's wait or another role's gave up) they may not have.
+        const uint32_t pending = issued < static_cast<uint32_t>(L::kStages) ? issued : L::kStages;
+        RingPos back = pos;
+        for (uint32_t i = 0; i < pending; ++i) {
+            back = back.stage == 0 ? RingPos{L::kStages - 1u, back.phase ^ 1u} : RingPos{back.stage - 1, back.phase};
+            mbar_wait_drain(bar(L::kKvFull + back.stage), back.phase, 50000000ull);
         }
+        for (int t = 0; t < 2; ++t)
+            if (q_issued & (1u << t)) mbar_wait_drain(bar(L::kQFull + t), q_parity, 50000000ull);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop and waits; one elected lane issues the
         // MMAs and commits (a converged warp issues tcgen05.mma faster than a
         // lone divergent lane).
-        constexpr uint32_t idesc_s = make_idesc_bf16_f32(kBr, kBc, false, false);
+        const uint32_t idesc_s = make_idesc_bf16_f32(kBr, kBc, false, false) | (p.negate_scores ? kIdescNegateB : 0u);
         constexpr uint32_t idesc_o = make_idesc_bf16_f32(kBr, D, false, true);
         // The descriptor's start-address field holds (address >> 4), so a move
         // inside shared memory is an add on the descriptor.
@@ -529,8 +626,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     mx3 = fmax3(mx3, s3[c], s3[c + 1]);
                 }
                 mx0 = fmax3(mx0, fmax3(mx2, s2[31], mx3), s3[31]);
-                const float m_tile = mx0 * sl2;
-                const bool grow = m_tile > m_ref + kRescaleLog2;
+                const float m_tile = mx0 * p.max_scale_log2;
+                const bool grow = m_tile > m_ref + kRescaleLog2Bf16;
                 float alpha = 1.f;
                 if (grow) {
                     alpha = ex2_approx(m_ref - m_tile);  // 0 on the first tile
@@ -548,10 +645,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         float x0, x1, x2, x3;  // exponents, two per packed instruction
                         ffma2(x0, x1, sc[2 * c], sc[2 * c + 1], sl2, -m_use);
                         ffma2(x2, x3, sc[2 * c + 2], sc[2 * c + 3], sl2, -m_use);
-                        const float a0 = ex2_approx(x0);
-                        const float b0 = ex2_approx(x1);
-                        const float a1 = ex2_approx(x2);
-                        const float b1 = ex2_approx(x3);
+                        float a0, b0, a1, b1;
+                        // the first kPolyPer32 scores of every 32 on the FMA pipes
+                        if (2 * c < kPolyPer32) {
+                            exp2_poly2(a0, b0, x0, x1);
+                        } else {
+                            a0 = ex2_approx(x0);
+                            b0 = ex2_approx(x1);
+                        }
+                        if (2 * c + 2 < kPolyPer32) {
+                            exp2_poly2(a1, b1, x2, x3);
+                        } else {
+                            a1 = ex2_approx(x2);
+                            b1 = ex2_approx(x3);
+                        }
                         fadd2(acc0, acc1, a0, b0);
                         fadd2(acc2, acc3, a1, b1);
                         pk[c] = pack_bf16x2(a0, b0);
@@ -615,9 +722,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
                 if (row_ok) p.LSE[grow_idx] = lse;
             } else {
-                // this segment's O / l (fp32) and LSE, merged later by the combine kernel
-                const size_t pidx = (static_cast<size_t>(item.u - p.split_first) * p.kv_split + item.seg) * (2 * kBr) +
-                                    t * kBr + rloc;
+                // This segment's O / l (fp32) and LSE go to the workspace; the
+                // segment that counts the row last merges the row's segments.
+                const int ord = item.u - p.split_first;  // the unit's place among the split units
+                const int rr = t * kBr + rloc;           // row within the pair
+                const size_t base = static_cast<size_t>(ord) * p.kv_split * (2 * kBr) + rr;  // segment s at base + s 2 kBr
+                const size_t pidx = base + static_cast<size_t>(item.seg) * (2 * kBr);
                 float4* orow = reinterpret_cast<float4*>(p.part_o + pidx * D);
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
@@ -631,7 +741,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                                           __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
                     }
                 }
-                if (row_ok) p.part_lse[pidx] = lse;
+                if (row_ok) {
+                    p.part_lse[pidx] = lse;
+                    // release this row's partial result, then count it; the
+                    // thread that counts last sees every segment's writes
+                    __threadfence();
+                    if (atomicAdd(p.part_count + static_cast<size_t>(ord) * (2 * kBr) + rr, 1) == item.nseg - 1) {
+                        __threadfence();
+                        merge_split_row<D>(p.part_o, p.part_lse, p.O, p.LSE, base, item.nseg, grow_idx);
+                    }
+                }
             }
             tc_fence_before_sync();
             mbar_arrive(bar(L::kOEmpty + t));
@@ -650,61 +769,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
-}
-
-// Merge the segments of the split units: per row, with the segments' partial
-// results (O_s = softmax over the segment's keys times V, LSE_s),
-//     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
-// the same online-softmax combination as inside the kernel, across segments.
-// One warp per row of the split units (2 kBr rows each); the rows of the other
-// units were written by the attention kernel itself.
-template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256) attn_fwd_combine_kernel(const FwdParams p) {
-    constexpr int kPer = D / 32;  // columns per lane
-    // launched as a programmatic dependent of the attention kernel: wait until
-    // that grid has completed and its writes are visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int prow = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);  // over split_units * 2 kBr
-    const int lane = threadIdx.x & 31;
-    if (prow >= p.split_units * 2 * kBr) return;
-    const int ord = prow / (2 * kBr);
-    const int rr = prow - ord * 2 * kBr;  // row within the pair: tile rr / kBr, row rr % kBr
-    const UnitInfo ui = decode_unit<CAUSAL>(p.split_first + ord, p);
-    const int qrow = ui.q0 * kBr + rr;
-    if (qrow >= p.N) return;
-    const size_t row = static_cast<size_t>(ui.bh) * p.N + qrow;
-    const int nseg = p.kv_split;
-    const size_t base = static_cast<size_t>(ord) * nseg * (2 * kBr) + rr;  // segment s at base + s * 2 kBr
-    float lse[kMaxKvSplit];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) {
-        lse[s] = s < nseg ? p.part_lse[base + s * (2 * kBr)] : -INFINITY;
-        mx = fmaxf(mx, lse[s]);
-    }
-    float wsum = 0.f;
-#pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) {
-        lse[s] = s < nseg ? expf(lse[s] - mx) : 0.f;  // now the segment weights
-        wsum += lse[s];
-    }
-    const float inv = 1.f / wsum;
-    float acc[kPer];
-#pragma unroll
-    for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
-#pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) {
-        if (s < nseg) {
-            const float* src = p.part_o + (base + s * (2 * kBr)) * D + lane * kPer;
-            const float ws = lse[s] * inv;
-#pragma unroll
-            for (int c = 0; c < kPer; ++c) acc[c] = fmaf(ws, src[c], acc[c]);
-        }
-    }
-    uint32_t* dst = reinterpret_cast<uint32_t*>(p.O + row * D + lane * kPer);
-#pragma unroll
-    for (int c = 0; c < kPer; c += 2) dst[c / 2] = pack_bf16x2(acc[c], acc[c + 1]);
-    if (lane == 0) p.LSE[row] = mx + logf(wsum);
 }
 
 }  // namespace elsattn

@@ -12,15 +12,31 @@
 //     K and V are streamed once per CTA  2 N d * ceil(N / (q Br))
 //     O is written once                  N d
 // so the streamed K/V term shrinks with the resident query rows q Br, and the
-// best tiling is the largest q Br that fits:
+// best tiling is the largest q Br the SM can run.  Br = 128 (one TMEM lane per
+// query row, tcgen05 M = 128).  The constraints:
 //     shared memory  q Br d 2B + stages Bc d 2B   <= 227 KB   (stages >= 3)
 //     tensor memory  q (Bc + d) fp32 columns       <= 512     (S and O per tile)
-// with Br = 128 (one TMEM lane per query row, tcgen05 M = 128).  The search
-// runs over every capacity-feasible (q, Bc); the plan reports the overall
-// I/O optimum and selects the least-traffic tiling among those the kernel
-// is compiled for (q = 2 query tiles in ping-pong, Bc = 128).  At d = 128 the
-// two coincide; at d = 64 the optimum is q = 4, Bc = 64, which the kernel
-// does not implement.
+//     registers      128 (q + 1) threads x (Bc + 40) <= 65536 (a softmax thread
+//                    holds its row's Bc scores plus about 40 of state; one
+//                    warpgroup besides the q softmax warpgroups loads and issues)
+//     tensor rate    S = Q K^T reads both operands from shared memory: per
+//                    16-deep step, 2 * 128 * Bc * 16 FLOP take Bc / 2 cycles at
+//                    8192 FLOP per cycle, and (128 + Bc) * 16 * 2 bytes take
+//                    (128 + Bc) / 4 cycles at 128 B per cycle; the product runs
+//                    at the full rate only for Bc >= 128 (O += P V reads P from
+//                    tensor memory and only V from shared memory: always full)
+// The planner searches every (q, Bc) and keeps the least I/O among the tilings
+// that meet all four (on a tie, the more resident rows, then the larger Bc).  That optimum is q = 2, Bc = 128
+// for both head dimensions, the tiling the kernel is compiled for.  Without the
+// tensor-rate constraint the count alone would favour Bc = 64 with three
+// resident tiles at d = 64, whose S products would run at two thirds of the
+// rate to save L2 -> shared-memory traffic that is nowhere near its bound.
+//
+// Device-memory traffic: each (batch, head)'s K and V come from HBM once when
+// the K/V of the heads streamed at the same time fit in the L2 budget (the
+// head-major order keeps the CTAs in flight on few heads; the causal order
+// runs heads in groups sized to that budget); beyond it, the share of the
+// re-reads that no longer hits L2 is charged to HBM as well.
 #include <cmath>
 
 #include "../../include/exact_attn.h"
@@ -28,10 +44,15 @@
 
 namespace elsattn {
 
+constexpr int kRegsPerSm = 65536;
+constexpr int kSoftmaxStateRegs = 40;  // registers of a softmax thread besides its row of scores
+constexpr double kL2KvBudget = 96.0 * 1024 * 1024;  // of the 126 MB L2, for K/V of the heads in flight
+
 struct Candidate {
     int q, Bc, stages;
     double l2_bytes;
-    bool fits;
+    bool fits;       // shared memory, tensor memory, registers
+    bool full_rate;  // S = Q K^T at the tensor core's full rate
 };
 
 // K/V bytes the CTAs stream from L2 for one (batch, head), plus Q read and O written.
@@ -44,12 +65,16 @@ static double l2_traffic_per_head(int N, int d, int q, int causal) {
 }
 
 static Candidate evaluate(int N, int d, int causal, int q, int Bc) {
-    Candidate c{q, Bc, 0, 0.0, false};
+    Candidate c{q, Bc, 0, 0.0, false, false};
     const int q_bytes = q * kBr * d * 2;
     const int stage_bytes = Bc * d * 2;
     const int tmem = q * (Bc + d);
+    const int threads = 128 * (q + 1);
+    const int regs = Bc + kSoftmaxStateRegs;
     c.stages = (kSmemLimit - overhead_bytes(0) - q_bytes) / (stage_bytes + 16);
-    c.fits = tmem <= 512 && c.stages >= 3;
+    c.fits = tmem <= 512 && c.stages >= 3 && regs <= 255 && threads * regs <= kRegsPerSm;
+    // per 16-deep step of S: Bc / 2 cycles of arithmetic against (128 + Bc) / 4 of operand reads
+    c.full_rate = 2 * Bc >= kBr + Bc;
     c.l2_bytes = l2_traffic_per_head(N, d, q, causal);
     return c;
 }
@@ -63,24 +88,24 @@ extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sm
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if (static_cast<long long>(B) * H * N >= (1LL << 31)) return ATTN_ERR_INVALID_ARG;
 
-    // Search the tilings the capacity allows; keep the one with least traffic
-    // overall, and the one with least traffic among the compiled variants.
-    Candidate best{0, 0, 0, 0.0, false}, chosen{0, 0, 0, 0.0, false};
-    auto better = [](const Candidate& c, const Candidate& b) {
-        // less traffic first, then the larger K/V tile (fewer pipeline steps)
-        return !b.fits || c.l2_bytes < b.l2_bytes * (1 - 1e-12) ||
-               (std::fabs(c.l2_bytes - b.l2_bytes) <= b.l2_bytes * 1e-12 && c.Bc > b.Bc);
-    };
+    // The least-traffic tiling among those the SM runs at the full tensor rate.
+    Candidate best{0, 0, 0, 0.0, false, false};
     const int qs[] = {1, 2, 3, 4};
     const int bcs[] = {64, 128, 256};
     for (int q : qs)
         for (int bc : bcs) {
             const Candidate c = evaluate(N, d, causal, q, bc);
-            if (!c.fits) continue;
-            if (better(c, best)) best = c;
-            if (q == kQTiles && bc == kBc && better(c, chosen)) chosen = c;
+            if (!c.fits || !c.full_rate) continue;
+            // less traffic first; on a tie (short sequences, where every tiling
+            // streams K/V once) more resident query rows, then the larger K/V
+            // tile (fewer pipeline steps)
+            const bool tie = std::fabs(c.l2_bytes - best.l2_bytes) <= best.l2_bytes * 1e-12;
+            if (!best.fits || (!tie && c.l2_bytes < best.l2_bytes) ||
+                (tie && (c.q > best.q || (c.q == best.q && c.Bc > best.Bc))))
+                best = c;
         }
-    if (!chosen.fits) return ATTN_ERR_UNSUPPORTED;
+    // The kernel is compiled for one tiling; the planner must arrive at it.
+    if (!best.fits || best.q != kQTiles || best.Bc != kBc) return ATTN_ERR_UNSUPPORTED;
     out->io_opt_q_tiles = best.q;
     out->io_opt_Bc = best.Bc;
     out->io_opt_l2_bytes = static_cast<double>(B) * H * best.l2_bytes + static_cast<double>(B) * H * 4.0 * N;
@@ -112,8 +137,24 @@ extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sm
     out->flops = 4.0 * BH * static_cast<double>(N) * N * d * (causal ? 0.5 : 1.0);
     out->io_bytes = BH * (2.0 * 4.0 * nd + 4.0 * N);
     out->l2_bytes = BH * l2_traffic_per_head(N, d, kQTiles, causal) + BH * 4.0 * N;
-    // HBM: each head's K/V comes from HBM once when the heads in flight fit in
-    // L2 (the schedule keeps them together), so the model is the I/O bound.
-    out->hbm_bytes = out->io_bytes;
+
+    // Heads whose K/V are streamed at the same time.  Non-causal, head-major:
+    // the grid's CTAs cover `grid` consecutive units, which span at most
+    // ceil(grid / pairs) + 1 heads.  Causal: one group of heads at a time (a
+    // group's K/V take half of the budget, which leaves room for the next
+    // group's heaviest units starting while the current group ends).
+    long long heads_in_flight;
+    if (!causal) {
+        heads_in_flight = (out->grid + pairs - 1) / pairs + 1;
+    } else {
+        heads_in_flight = g;
+    }
+    if (heads_in_flight > BH) heads_in_flight = BH;
+    out->kv_in_flight_bytes = static_cast<double>(heads_in_flight) * kv_head_bytes;
+    out->l2_fit = out->kv_in_flight_bytes <= kL2KvBudget ? 1.0 : kL2KvBudget / out->kv_in_flight_bytes;
+    // HBM: K/V once per head, plus the share of the re-reads that misses L2.
+    const double kv_once = BH * 2.0 * 2.0 * nd;
+    const double kv_streamed = out->l2_bytes - BH * (2.0 * 2.0 * nd + 4.0 * N);
+    out->hbm_bytes = out->io_bytes + (1.0 - out->l2_fit) * (kv_streamed - kv_once);
     return ATTN_OK;
 }

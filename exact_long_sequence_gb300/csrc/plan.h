@@ -2,9 +2,9 @@
 //
 // The kernel keeps kQTiles query tiles of kBr rows resident per CTA and
 // streams K/V tiles of kBc keys through a shared-memory ring.  These numbers
-// are what the planner's I/O count selects for an sm_103 SM (see plan.cpp);
-// they are compile-time constants here because the kernel is specialised on
-// them.
+// are what the planner's I/O count selects for an sm_103 SM at both head
+// dimensions (plan.cpp, which checks that it does); they are compile-time
+// constants here because the kernel is specialised on them.
 #pragma once
 
 #include <cstdint>

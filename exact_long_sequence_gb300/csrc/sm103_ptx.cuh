@@ -173,6 +173,9 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16_f32(int M, int N, bool a_
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Instruction-descriptor bit that negates the B operand (bit 14; bit 13 negates A).
+constexpr uint32_t kIdescNegateB = 1u << 14;
+
 // Instruction descriptor, kind::f8f6f4 with E4M3 A and B (type code 0) and an
 // fp32 accumulator; both operands K-major.
 __host__ __device__ constexpr uint32_t make_idesc_e4m3_f32(int M, int N) {
@@ -287,6 +290,12 @@ __device__ __forceinline__ void tmem_wait_st() {
 #undef ELS_R8
 #undef ELS_U8
 #undef ELS_I8
+
+// Invalidate one 128-byte line of global memory in L2 without writing it back
+// (its contents become undefined): for scratch data that nothing reads again.
+__device__ __forceinline__ void l2_discard_line(const void* line128) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(line128) : "memory");
+}
 
 // ---------------------------------------------------------------------------
 // Scalar helpers

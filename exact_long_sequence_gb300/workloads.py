@@ -81,8 +81,8 @@ def _draw(B: int, H: int, N: int, d: int, seed: int, qk_dist: str, v_dist: str):
     if qk_dist == "normal_spiky":
         mq = torch.rand(shape, generator=g) < 0.01
         mk = torch.rand(shape, generator=g) < 0.01
-        q[mq] *= 10
-        k[mk] *= 10
+        q = torch.where(mq, q * 10, q)
+        k = torch.where(mk, k * 10, k)
     elif qk_dist != "normal":
         raise ValueError(qk_dist)
     return q, k, v

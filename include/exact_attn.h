@@ -39,7 +39,7 @@ extern "C" {
 
 typedef enum {
     ATTN_OK = 0,
-    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, non-finite or non-positive scale */
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, or a scale out of range (see each call) */
     ATTN_ERR_UNSUPPORTED = 2,  /* head dim other than 64/128, or a device other than sm_103 */
     ATTN_ERR_MISALIGNED = 3,   /* a tensor base address is not 16-byte aligned */
     ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed: see attn_last_cuda_error() */
@@ -65,10 +65,13 @@ typedef struct {
     double flops;         /* 4*B*H*N^2*d, halved when causal */
     double io_bytes;      /* Theta(N*d) bound: bf16 Q,K,V read + bf16 O, fp32 LSE written once */
     double l2_bytes;      /* modelled L2->SMEM traffic of the chosen tiling */
-    double hbm_bytes;     /* modelled HBM traffic of the chosen tiling and schedule */
-    int io_opt_q_tiles;   /* the capacity-feasible tiling with least L2->SMEM traffic ... */
-    int io_opt_Bc;        /* ... (may be one the kernel is not compiled for) */
-    double io_opt_l2_bytes; /* its modelled L2->SMEM traffic */
+    double hbm_bytes;     /* modelled HBM traffic: io_bytes, plus the K/V re-reads that miss L2 when
+                             the K/V of the heads in flight exceed the L2 budget */
+    int io_opt_q_tiles;   /* the tiling with least L2->SMEM traffic among those the SM runs at the   */
+    int io_opt_Bc;        /* full tensor rate within its shared memory, tensor memory and registers */
+    double io_opt_l2_bytes; /* its modelled L2->SMEM traffic (the kernel runs this tiling) */
+    double kv_in_flight_bytes; /* K/V bytes of the heads the schedule streams at the same time */
+    double l2_fit;        /* fraction of those that fit the L2 budget (1: every head's K/V read once) */
 } attn_plan_t;
 
 /*
@@ -79,7 +82,10 @@ typedef struct {
  *   LSE     : fp32 [B,H,N] device pointer, 4-byte aligned (written; natural log)
  *   B, H, N : >= 1 with B*H*N < 2^31;  d : 64 or 128
  *   causal  : 0 = no mask, nonzero = causal mask (key j visible to query i iff j <= i)
- *   scale   : finite, > 0 (typically 1/sqrt(d))
+ *   scale   : any finite value (typically 1/sqrt(d)).  A negative scale is run
+ *             as |scale| on the negated scores (the tensor core's negate bit), so
+ *             the running maximum tracks the largest scaled score; zero gives
+ *             the plain average of the visible values (LSE = ln #visible).
  *   stream  : CUDA stream on the current device (0 = legacy default stream)
  * Returns ATTN_OK when the launch was queued.  Kernel-side timeouts are
  * reported later by attn_last_device_error().
@@ -112,20 +118,26 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
  * every key they see.
  *   - Fewer units than SMs (few heads, or a causal mask whose longest query
  *     tiles dominate): the K/V range of the heaviest units is cut into
- *     segments that run on the SMs the units leave idle.
+ *     segments, either run on the SMs the units leave idle (one wave), or,
+ *     for a causal mask, claimed dynamically with the other units (below),
+ *     whichever the host's schedule estimate finds shorter.
  *   - More equal units than SMs (no mask): the units of the last, partial wave
  *     are cut into segments that spread over all SMs.
  *   - More causal units than SMs (units of unequal length): no segments; the
  *     persistent CTAs claim units dynamically, heaviest first, from a counter
- *     in `workspace` that this call zeroes on `stream` first.  Every unit is
- *     computed exactly as by attn_fwd, so the outputs are bit-identical to it.
+ *     in `workspace`.  Every unit is computed exactly as by attn_fwd, so the
+ *     outputs are bit-identical to it.
  * A segment is a work item of its own: it writes its partial result (O over
- * the segment's keys, normalised, fp32, and that segment's LSE) to `workspace`,
- * and a second kernel on `stream` merges the segments of each row by
+ * the segment's keys, normalised, fp32, and that segment's LSE) to `workspace`
+ * and counts itself in a per-row counter there; the segment that counts a row
+ * last merges the row's segments, in the same kernel, by
  *     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
  * the combination step of the online softmax (the streaming reformulation of
- * the IO-Aware Algorithms page) applied across segments.  The result is the same
- * operation as attn_fwd, up to floating-point rounding.
+ * the IO-Aware Algorithms page) applied across segments, and then drops the
+ * partial rows from L2 without writing them back.  The result is the same
+ * operation as attn_fwd, up to floating-point rounding.  The call zeroes the
+ * schedule counter and the per-row counters with a memset on `stream` before
+ * the kernel: one memset and one kernel launch.
  *   arguments as attn_fwd, plus
  *   workspace       : device buffer of at least attn_fwd_split_workspace_bytes()
  *                     bytes, 16-byte aligned, owned by the caller, not used by
@@ -173,7 +185,7 @@ int attn_fwd_split_choice(int B, int H, int N, int d, int causal, int num_sms, i
  *                    [B,H,N,d], then the row statistics -scale * D and
  *                    -LSE * log2(e) (negated for the kernel's packed FMAs) on rows
  *                    padded to a multiple of 128 per (batch, head)
- * Same size, alignment and error rules as attn_fwd; asynchronous on `stream`.
+ * Same size, alignment, scale and error rules as attn_fwd; asynchronous on `stream`.
  */
 int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
              void* dK, void* dV, int B, int H, int N, int d, int causal, float scale, void* workspace,
@@ -187,9 +199,12 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 /*
  * attn_plan - host only, launches nothing.  Fills *out with the tiling the
  * planner derives from an I/O count of the two tall-and-skinny products
- * (S = Q K^T and O = P V) against the shared- and tensor-memory capacity of an
- * sm_103 SM (the I/O-optimal tiling of the AttenIO abstract, "I/O Analysis
- * is All You Need", ASPLOS 2026).  num_sms <= 0 queries the current device.
+ * (S = Q K^T and O = P V): the least-traffic tiling among those an sm_103 SM
+ * holds (shared memory, tensor memory, registers) and runs at the full tensor
+ * rate (the I/O-optimal tiling of the AttenIO abstract, "I/O Analysis is All
+ * You Need", ASPLOS 2026).  That is the tiling the kernel is compiled for;
+ * ATTN_ERR_UNSUPPORTED if it ever were not.  num_sms <= 0 queries the current
+ * device.
  */
 int attn_plan(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out);
 
@@ -215,6 +230,22 @@ const char* attn_strerror(int status);
 int attn_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
 
 /*
+ * attn_debug_arm_timeout - test hook for the forward kernel's own abort path
+ * (every wait is bounded: a role whose wait runs out records ATTN_ERR_TIMEOUT,
+ * the other roles leave their loops, in-flight copies and MMAs are drained
+ * and tensor memory is freed before the kernel returns).  Arms a one-shot:
+ * the next forward launch of this process (attn_fwd, attn_fwd_split,
+ * attn_fwd_noalloc; the first chunk of attn_fwd_host) runs with a wait limit
+ * of timeout_ns (1 us .. 1 s) instead of 4 s, and its CTA 0 arms the barrier
+ * of its first query-tile copy without issuing the copy, so the wait on it
+ * runs out.  That launch's outputs are left partly unwritten; the status is
+ * read with attn_last_device_error() (attn_noalloc_last_device_error() after
+ * attn_fwd_noalloc).  Launches after it are normal.  ATTN_ERR_INVALID_ARG for
+ * a limit out of range.  Not for production use.
+ */
+int attn_debug_arm_timeout(uint64_t timeout_ns);
+
+/*
  * attn_fwd_noalloc - attn_fwd for callers that must not let the library
  * allocate device memory: applications that reserve all of device memory for
  * their own pool up front (such as a server handing the rest of HBM to its
@@ -235,12 +266,21 @@ int attn_debug_wait_timeout(uint64_t timeout_ns, cudaStream_t stream);
  *   - Every call shares the one array and clears its error word before the
  *     launch.  Calls that overlap on the GPU (other streams, other threads)
  *     race on that word; serialise them.
- *   - A kernel-side timeout is recorded in the array, not in the word that
- *     attn_last_device_error reads.
+ *   - A kernel-side timeout is recorded in the array: read it with
+ *     attn_noalloc_last_device_error() before the next call clears it.
  * Returns the same status codes as attn_fwd.
  */
 int attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d,
                      int causal, float scale, cudaStream_t stream);
+
+/*
+ * attn_noalloc_last_device_error - the error word of attn_fwd_noalloc: waits
+ * for `stream`, then reads the word in the fixed array and clears it (an
+ * asynchronous copy and memset on `stream`, each waited for); allocates
+ * nothing.  Returns ATTN_OK or ATTN_ERR_TIMEOUT for the most recent
+ * attn_fwd_noalloc on the current device, or a set-up error (as attn_fwd_noalloc).
+ */
+int attn_noalloc_last_device_error(cudaStream_t stream);
 
 /*
  * attn_fwd_fp8 - the same forward on 8-bit inputs (the FP8 variant that the
@@ -257,7 +297,7 @@ int attn_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float
  * zeroes on `stream`; each unit is computed as under the static schedule.
  *   Q8, K8, V8 : const uint8 [B,H,N,d] E4M3 codes, device, 16-byte aligned
  *   O, LSE     : as attn_fwd
- *   q_scale, k_scale, v_scale : finite and > 0
+ *   scale, q_scale, k_scale, v_scale : finite and > 0
  *   workspace  : device buffer of at least attn_fwd_fp8_workspace_bytes(), 16-byte
  *                aligned, owned by the caller, not used by other work while this
  *                call runs: V transposed to [B,H,d,N] (rows padded to 16 bytes),

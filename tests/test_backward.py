@@ -31,15 +31,16 @@ def built():
     ela.load_library()
 
 
-def check(B, H, N, d, causal, seed, oracle_mod, label):
+def check(B, H, N, d, causal, seed, oracle_mod, label, scale=None):
     q, k, v = workloads.make_inputs(B, H, N, d, seed=seed)
     do = workloads.make_inputs(B, H, N, d, seed=seed + 1000)[0]
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
-    o, lse = ela.attn_fwd(qd, kd, vd, causal=causal)
-    dq, dk, dv = ela.attn_bwd(qd, kd, vd, o, lse, dod, causal=causal)
+    scale = ela.default_scale(d) if scale is None else scale
+    o, lse = ela.attn_fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = ela.attn_bwd(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
     torch.cuda.synchronize()
     assert ela.last_device_error() == ela.ATTN_OK
-    ref = oracle_mod.attention_bwd(q, k, v, do, causal, ela.default_scale(d))
+    ref = oracle_mod.attention_bwd(q, k, v, do, causal, scale)
     for name, g, r in (("dQ", dq, ref[0]), ("dK", dk, ref[1]), ("dV", dv, ref[2])):
         gg = g.double().cpu().numpy().reshape(r.shape)
         assert np.isfinite(gg).all(), f"{label} {name}: non-finite"
@@ -58,6 +59,14 @@ def test_backward_parity_small(oracle_mod, N, causal, d):
 @pytest.mark.parametrize("causal", [False, True])
 def test_backward_parity_medium(oracle_mod, causal):
     check(1, 2, 2048, 128, causal, 300, oracle_mod, f"N=2048 causal={causal}")
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_negative_and_zero_scale(oracle_mod, scale, causal):
+    """P is recomputed from the forward's LSE and masked after the exponential, so the
+    backward takes any finite scale as it stands."""
+    check(1, 2, 300, 64, causal, 250, oracle_mod, f"scale={scale} causal={causal}", scale=scale)
 
 
 def test_backward_many_heads(oracle_mod):

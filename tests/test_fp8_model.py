@@ -35,6 +35,7 @@ import pytest
 import torch
 
 from exact_long_sequence_gb300 import workloads
+from fp8_bound import NEAR_CEILING_OFFSETS, fp8_output_bounds, near_ceiling_inputs
 
 LOG2E = 1.4426950408889634
 BC = 128
@@ -94,12 +95,7 @@ def bound_and_reference(oracle_mod, q8, k8, v8, scales, rows, causal, scale):
                                        rows=rows.numpy()[None], return_probs=True)
     O, L, P = O[0], L[0], P[0]
     vabs = np.abs(oracle_mod.decode_e4m3(v8, scales[2]))
-    loose = (2.0 ** -4 * P @ vabs + 2.0 ** -10 * vabs.sum(0)[None, :] * P.max(1)[:, None]
-             + 2.0 ** -8 * np.abs(O) + 1e-6)
-    pmax = P.max(1, keepdims=True)
-    p = P / pmax
-    e = np.where(p >= 2.0 ** -6, 2.0 ** -4 * p, np.minimum(p, 2.0 ** -10))
-    tight = (e @ vabs) * pmax + 2.0 ** -8 * np.abs(O) + 1e-6
+    loose, tight = fp8_output_bounds(P, vabs, O)
     return O, L, loose, tight
 
 
@@ -141,3 +137,20 @@ def test_a_threshold_beyond_e4m3_range_breaks_the_per_term_bound(oracle_mod, cas
     err = np.abs(O - O_ref)
     assert (err > tight).any()
     assert (err <= loose).all()  # the loose bound misses it
+
+
+def test_near_ceiling_terms_meet_the_bound_and_a_larger_threshold_saturates(oracle_mod):
+    """The planted case's terms reach 2^8 (the stale reference at the threshold): exact rounding
+    meets the per-term bound; a threshold of 16 lets the offsets above 8 reach 2^9 .. 2^12, which
+    saturate at 448 and break it."""
+    q8, k8, v8, scales, scale = near_ceiling_inputs()
+    rows = torch.arange(256)
+    O_ref, L_ref, loose, tight = bound_and_reference(oracle_mod, q8[0, 0], k8[0, 0], v8[0, 0], scales, rows,
+                                                     False, scale)
+    O, L = fp8_forward_replay(q8[0, 0], k8[0, 0], v8[0, 0], scales, rows, False, scale)
+    assert (np.abs(O - O_ref) <= tight).all()
+    assert (np.abs(L - L_ref) <= 1e-3 * np.abs(L_ref)).all()
+    O16, _ = fp8_forward_replay(q8[0, 0], k8[0, 0], v8[0, 0], scales, rows, False, scale, T=16.0)
+    bad = (np.abs(O16 - O_ref) > tight).any(1)
+    offsets = np.array(NEAR_CEILING_OFFSETS * (256 // len(NEAR_CEILING_OFFSETS)))
+    assert bad.any() and (offsets[bad] > 8.8).all()

@@ -1,14 +1,17 @@
 """GPU parity of the K/V split (attn_fwd_split).
 
 Problems with fewer work units than SMs cut the K/V range of their long units
-into segments that run on different CTAs; a second kernel merges the segments'
-partial results of each row by their LSE weights.  The result is the same
-operation as attn_fwd, so the forward's tolerances apply unchanged: against the
-fp64 oracle max |dO| <= 2e-2 and per-row |dLSE| <= 1e-3 |LSE|.  The shapes below
-are chosen so that the launch splits units into 2, 3 and 4 segments on a
+into segments that run on different CTAs; the segment that finishes a row last
+merges the row's partial results by their LSE weights, in the kernel.  Causal
+problems may take the dynamic schedule for their segments.  The result is the
+same operation as attn_fwd, so the forward's tolerances apply unchanged: against
+the fp64 oracle max |dO| <= 2e-2 and per-row |dLSE| <= 1e-3 |LSE|.  The shapes
+below are chosen so that the launch splits units into 2, 3 and 4 segments on a
 152-SM GB300 (the test checks the split the library reports is the expected
-one), with causal masks, ragged lengths, several schedule groups, and units
-left whole beside split ones.
+one), with causal masks, ragged lengths, several schedule groups, units left
+whole beside split ones, and split items claimed dynamically.  A second launch
+into fresh outputs with the same workspace must give the same bits (the
+per-row segment counts start from zero on every launch).
 
 Causal problems with more units than SMs take the same entry's dynamic
 schedule instead: CTAs claim units from a counter in the workspace.  Each unit
@@ -44,7 +47,9 @@ def chosen_split(B, H, N, d, causal):
 # units than SMs, the heaviest units are split, as many as the idle SMs allow.
 # With more (equal, non-causal) units, the units of the last partial wave are.
 CASES = [
-    (1, 8, 4096, 64, True, 2),     # the causal d = 64 workload: 128 units, the 24 heaviest split
+    (1, 8, 4096, 64, True, 2),     # the causal d = 64 workload: 128 units, 120 halved, claimed dynamically
+    (1, 4, 6000, 128, True, 3),    # ragged causal, 84 of 96 units in thirds, claimed dynamically
+    (3, 1, 7000, 64, True, 3),     # ragged causal, three schedule groups, dynamic
     (1, 2, 8192, 128, False, 2),   # 64 equal units, all split
     (1, 1, 1000, 64, False, 3),    # 4 units of 8 K/V tiles, ragged length
     (1, 5, 3000, 64, True, 3),     # ragged causal, 60 units of which 45 split
@@ -64,10 +69,15 @@ def test_split_parity(oracle_mod, B, H, N, d, causal, segs):
     assert chosen_split(B, H, N, d, causal) == segs
     q, k, v = workloads.make_inputs(B, H, N, d, seed=900 + N + H)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o, lse = ela.attn_fwd(qd, kd, vd, causal=causal)
+    ws = torch.empty(ela.split_workspace_bytes(B, H, N, d, causal), dtype=torch.uint8, device="cuda")
+    o, lse = ela.attn_fwd(qd, kd, vd, causal=causal, workspace=ws)
+    o2 = torch.full_like(o, float("nan"))
+    lse2 = torch.full_like(lse, float("nan"))
+    ela.attn_fwd(qd, kd, vd, causal=causal, workspace=ws, out=o2, lse=lse2)
     o1, lse1 = ela.attn_fwd(qd, kd, vd, causal=causal, split=False)
     torch.cuda.synchronize()
     assert ela.last_device_error() == ela.ATTN_OK
+    assert torch.equal(o, o2) and torch.equal(lse, lse2), "a second launch on the same workspace differs"
     # every row of the small cases, sampled rows (with the first and last) of the long ones
     R = N if B * H * N <= 16384 else 48
     rows = None

@@ -1,16 +1,20 @@
 """Host logic of the work split (attn_fwd_split_choice; no GPU needed).
 
-attn_fwd_split picks, per launch, one of three schedules:
-  - fewer units than SMs: the heaviest units are cut into segments of K/V tiles
-    on the SMs the units leave idle (one wave);
+attn_fwd_split picks, per launch, one of these schedules:
+  - fewer units than SMs: the heaviest units are cut into segments of K/V tiles,
+    either on the SMs the units leave idle (one wave, static), or, for causal
+    launches, as many as pays under the dynamic schedule (CTAs claim the items,
+    heaviest first);
   - more equal (non-causal) units than SMs: the units of the last, partial wave
     are cut into segments that spread over all SMs;
   - more causal units than SMs: no split, the dynamic schedule.
+The segment that finishes a row last merges the row's segments in the kernel.
 These tests pin the choices for the benchmark workloads, and check over a
 sweep of shapes and SM counts that every choice is one the kernel can run: each
 segment of each split unit holds at least one K/V tile of both query tiles
-(the kernel's own segment arithmetic), a split of an under-filled launch stays
-one wave, and a split and the dynamic schedule are never combined.
+(the kernel's own segment arithmetic), a static split of an under-filled launch
+stays one wave, and a split takes the dynamic schedule only for a causal launch
+with fewer units than SMs.
 """
 import ctypes
 
@@ -54,7 +58,7 @@ def unit_tiles(u, BH, N, causal, G):
 # (B, H, N, d, causal) -> (segments, first split unit, split units, dynamic) on 152 SMs
 PINNED = {
     (1, 1, 256, 64, False): (1, 0, 0, 0),        # C1: one unit of two K/V tiles
-    (1, 8, 4096, 64, True): (2, 0, 24, 0),       # C2: the 24 heaviest of 128 units
+    (1, 8, 4096, 64, True): (2, 0, 120, 1),      # C2: 120 of 128 units halved, 248 items claimed dynamically
     (1, 16, 16384, 128, False): (4, 912, 112, 0),  # C3: the last partial wave (1024 = 6 * 152 + 112)
     (1, 8, 65536, 128, True): (1, 0, 0, 1),      # C4: dynamic schedule
     (4, 32, 8192, 128, True): (1, 0, 0, 1),      # C5: dynamic schedule
@@ -77,7 +81,7 @@ def test_pinned_choices(lib, shape):
 
 
 def test_choices_are_runnable_over_a_sweep(lib):
-    checked = splits = 0
+    checked = splits = dyn_splits = 0
     for sms in (132, 148, 152, 160):
         for B, H in ((1, 1), (1, 3), (2, 5), (1, 8), (4, 16)):
             for N in (128, 300, 1000, 2048, 4096, 9000, 16384):
@@ -91,9 +95,11 @@ def test_choices_are_runnable_over_a_sweep(lib):
                             assert units == 0
                         else:
                             splits += 1
-                            assert not dyn, "a split and the dynamic schedule together"
                             assert units >= 1 and first >= 0 and first + units <= p.num_units
-                            if p.num_units < sms:
+                            if dyn:
+                                dyn_splits += 1
+                                assert causal and p.num_units < sms and first == 0
+                            elif p.num_units < sms:
                                 assert first == 0 and p.num_units + units * (segs - 1) <= sms  # one wave
                             else:
                                 assert not causal and first == p.num_units - p.num_units % sms
@@ -103,8 +109,11 @@ def test_choices_are_runnable_over_a_sweep(lib):
                                 for s in range(segs):
                                     jb, je = s * c, min(n1, s * c + c)
                                     assert jb < min(je, n0), (B, H, N, causal, sms, u, s)
-                        assert dyn == (1 if causal and p.num_units > sms else 0)
-    assert checked == 4 * 5 * 7 * 2 * 2 and splits > 20
+                        if p.num_units > sms:
+                            assert dyn == (1 if causal else 0)
+                        else:
+                            assert dyn == 0 or segs > 1
+    assert checked == 4 * 5 * 7 * 2 * 2 and splits > 20 and dyn_splits > 5
 
 
 def test_invalid_arguments(lib):
