@@ -11,7 +11,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libexact_attn.so")
-SOURCES = ["api_common.cu", "attn_api.cu", "attn_bwd_api.cu", "attn_fp8_api.cu", "rowwise_api.cu", "plan.cpp"]
+SOURCES = ["api_common.cu", "attn_api.cu", "attn_bwd_api.cu", "attn_fp8_api.cu", "rowwise_api.cu", "plan.cpp",
+           "split_policy.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

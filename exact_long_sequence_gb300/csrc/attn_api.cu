@@ -22,6 +22,7 @@
 #include "api_common.h"
 #include "attn_fwd_kernel.cuh"
 #include "plan.h"
+#include "split_policy.h"
 
 extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out);
 
@@ -73,185 +74,31 @@ int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, con
     kernel<<<grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
+    if (p.kv_split > 1) {
+        // programmatic dependent launch: the combine kernel's CTAs may start as the
+        // attention kernel's retire, and wait in-kernel for its completion
+        const int rows = p.split_units * 2 * kBr;  // the rows of the split units
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, attn_fwd_combine_kernel<D, CAUSAL>, p)) != cudaSuccess) return cuda_fail(e);
+    }
     return ATTN_OK;
 }
 
-// Units the split policy considers (a launch with more units than SMs is not split).
-constexpr int kMaxUnitsForSplit = 1024;
 
-struct KvSplit {
-    int segs;      // segments per split unit (1: no split)
-    int units;     // how many units are split ...
-    int first;     // ... starting at this unit in schedule order
-    bool dynamic;  // CTAs claim work items from a counter instead of a fixed stride
-};
-
-// Per-item cost besides its K/V steps (Q load, pipeline fill, epilogue), in K/V
-// steps of a query-tile pair (one step measured at about 1.2 us).
-constexpr int kItemSteps = 2;
-// Extra cost of a segment: its partial result goes out in fp32, and the last
-// segment of each row reads the row's partials back and merges them.
-constexpr int kMergeSteps = 1;
-
-// Greedy list scheduling of work items of the given costs (in order) on `grid`
-// CTAs: CTA i starts with item i, then every further item goes to the CTA that
-// becomes free first, as the dynamic schedule's counter hands them out.
-// Returns the time the last CTA finishes.
-int greedy_makespan(const int* cost, int items, int grid) {
-    std::priority_queue<int, std::vector<int>, std::greater<int>> free_at;
-    int i = 0;
-    for (; i < items && i < grid; ++i) free_at.push(cost[i]);
-    int end = 0;
-    for (; i < items; ++i) {
-        const int t = free_at.top();
-        free_at.pop();
-        free_at.push(t + cost[i]);
-    }
-    while (!free_at.empty()) {
-        end = free_at.top() > end ? free_at.top() : end;
-        free_at.pop();
-    }
-    return end;
-}
-
-// The work schedule of attn_fwd_split for a launch on num_sms SMs; one K/V
-// step is one K/V tile for a query-tile pair.
-//   - More causal units than SMs: the dynamic schedule, no split.
-//   - More non-causal (equal) units than SMs: the units of the last, partial
-//     wave are split so that their segments spread over all SMs.
-//   - Fewer units than SMs: the heaviest units (a prefix in the kernel's
-//     schedule order, decode_unit) are cut into s segments.  Either the split
-//     stays one wave on the SMs the units leave idle (static), or, for causal
-//     launches, any number of units are split and the CTAs claim the items
-//     dynamically, heaviest first (greedy_makespan estimates it).
-// A unit takes s segments only when s (s - 1) < n0 (see decode_item).  The
-// estimate with the least time wins; no split when none beats the unsplit one.
-KvSplit choose_kv_split_uncached(const attn_plan_t& plan, int num_sms, int BH, int N, int causal) {
-    KvSplit best{1, 0, 0, false};
-    const int units = plan.num_units;
-    if (units < 1) return best;
-    if (units >= num_sms) {
-        if (causal) return KvSplit{1, 0, 0, units > num_sms};
-        // The static stride gives every CTA q = units / num_sms units and R =
-        // units % num_sms CTAs one more, a last wave that leaves the other SMs
-        // idle.  Splitting those R units into s segments spreads the last wave
-        // over all SMs: the first units - R items are whole (q per CTA), then
-        // come R * s segments in turn.
-        const int L = (N + kBc - 1) / kBc;  // K/V steps of every unit
-        const int q = units / num_sms, R = units % num_sms;
-        if (R == 0) return best;
-        int best_cost = (q + 1) * (L + kItemSteps);
-        for (int s = 2; s <= kMaxKvSplit; ++s) {
-            if (s * (s - 1) >= L) break;
-            const int pieces_per_sm = (R * s + num_sms - 1) / num_sms;
-            const int cost = q * (L + kItemSteps) + pieces_per_sm * ((L + s - 1) / s + kItemSteps + kMergeSteps);
-            if (cost < best_cost) {
-                best_cost = cost;
-                best = KvSplit{s, R, units - R, false};
-            }
-        }
-        return best;
-    }
-    if (units > kMaxUnitsForSplit) return best;
-    const int nq = (N + kBr - 1) / kBr, nkv = (N + kBc - 1) / kBc, pairs = (nq + 1) / 2;
-    const int G = plan.heads_per_group > 0 ? plan.heads_per_group : 1;
-    std::vector<int> n0(units), n1(units);
-    int longest = 0;
-    for (int u = 0; u < units; ++u) {
-        int pair;
-        if (!causal) {
-            pair = u % pairs;
-        } else {
-            const int g = u / (G * pairs), r = u - g * G * pairs;
-            const int heads_here = (BH - g * G) < G ? (BH - g * G) : G;
-            pair = pairs - 1 - r / heads_here;
-        }
-        const int q0 = 2 * pair;
-        n0[u] = causal ? (q0 + 1 < nkv ? q0 + 1 : nkv) : nkv;
-        n1[u] = causal ? (q0 + 2 < nkv ? q0 + 2 : nkv) : nkv;
-        if (n1[u] > longest) longest = n1[u];
-    }
-    int best_cost = longest + kItemSteps;
-    std::vector<int> cost(units * kMaxKvSplit);
-    for (int s = 2; s <= kMaxKvSplit; ++s) {
-        int Umax = 0;  // the longest prefix of units that can take s segments
-        while (Umax < units && s * (s - 1) < n0[Umax]) ++Umax;
-        if (Umax == 0) continue;
-        // one wave: only the idle SMs take the extra segments
-        const int U1 = std::min(Umax, (num_sms - units) / (s - 1));
-        if (U1 > 0) {
-            int c = 0;
-            for (int u = 0; u < units; ++u) {
-                const int steps = u < U1 ? (n1[u] + s - 1) / s + kMergeSteps : n1[u];
-                c = std::max(c, steps + kItemSteps);
-            }
-            if (c < best_cost) {
-                best_cost = c;
-                best = KvSplit{s, U1, 0, false};
-            }
-        }
-        if (!causal) continue;
-        // dynamic: every prefix length at which the split units' length changes
-        for (int U = 1; U <= Umax; ++U) {
-            if (U < Umax && n1[U] == n1[U - 1]) continue;
-            int items = 0;
-            for (int u = 0; u < units; ++u) {
-                if (u < U) {
-                    const int c = (n1[u] + s - 1) / s;
-                    for (int seg = 0; seg < s; ++seg) {
-                        const int jb = seg * c, je = std::min(n1[u], jb + c);
-                        cost[items++] = (je - jb) + kItemSteps + kMergeSteps;
-                    }
-                } else {
-                    cost[items++] = n1[u] + kItemSteps;
-                }
-            }
-            const int c = greedy_makespan(cost.data(), items, std::min(items, num_sms));
-            if (c < best_cost) {
-                best_cost = c;
-                best = KvSplit{s, U, 0, true};
-            }
-        }
-    }
-    return best;
-}
-
-// The choice for a shape is computed once and kept (the dynamic candidates
-// take a few hundred simulations of the item schedule).
-KvSplit choose_kv_split(const attn_plan_t& plan, int num_sms, int BH, int N, int causal) {
-    static std::mutex m;
-    static std::map<std::tuple<int, int, int, int, int, int>, KvSplit> cache;
-    const auto key = std::make_tuple(BH, N, plan.heads_per_group, plan.num_units, causal, num_sms);
-    {
-        std::lock_guard<std::mutex> lock(m);
-        const auto it = cache.find(key);
-        if (it != cache.end()) return it->second;
-    }
-    const KvSplit s = choose_kv_split_uncached(plan, num_sms, BH, N, causal);
-    std::lock_guard<std::mutex> lock(m);
-    if (cache.size() >= 4096) cache.clear();
-    cache.emplace(key, s);
-    return s;
-}
-
-// Workspace of attn_fwd_split: [256 B: the schedule counter][per-row segment
-// counts of the split units][O partials][LSE partials], each part 256-aligned.
-constexpr size_t kCounterBlock = 256;
-
-size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
-
-size_t split_count_bytes(const KvSplit& s) { return align256(static_cast<size_t>(s.units) * (2 * kBr) * 4); }
-
-size_t split_part_o_bytes(const KvSplit& s, int d) {
-    return align256(static_cast<size_t>(s.units) * s.segs * (2 * kBr) * d * 4);
-}
-
+// Workspace of attn_fwd_split: [256 B: the schedule counter][O partials][LSE
+// partials], each part 256-aligned.
 size_t split_workspace_bytes(const KvSplit& s, int d) {
     if (s.segs <= 1 && !s.dynamic) return 0;
-    size_t b = kCounterBlock;
-    if (s.segs > 1)
-        b += split_count_bytes(s) + split_part_o_bytes(s, d) + static_cast<size_t>(s.units) * s.segs * (2 * kBr) * 4;
-    return b;
+    return kCounterBlock + split_part_o_bytes(s, d) + split_part_lse_bytes(s);
 }
 
 int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int d, int causal,
@@ -293,15 +140,11 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     p.split_units = split.units;
     p.num_items = plan.num_units + split.units * (kv_split - 1);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const size_t counts = kv_split > 1 ? split_count_bytes(split) : 0;
-    p.part_count = kv_split > 1 ? reinterpret_cast<int*>(ws + kCounterBlock) : nullptr;
-    p.part_o = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + counts) : nullptr;
-    p.part_lse =
-        kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + counts + split_part_o_bytes(split, d)) : nullptr;
+    p.part_o = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock) : nullptr;
+    p.part_lse = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + split_part_o_bytes(split, d)) : nullptr;
     p.sched_counter = dynamic ? reinterpret_cast<int*>(ws) : nullptr;
-    if (dynamic || kv_split > 1) {
-        // the schedule counter and the per-row segment counts start at zero
-        cudaError_t e = cudaMemsetAsync(ws, 0, dynamic && kv_split == 1 ? sizeof(int) : kCounterBlock + counts, stream);
+    if (dynamic) {
+        cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), stream);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     take_armed_hook(p);

@@ -13,6 +13,7 @@
 #include "attn_fwd_fp8_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "plan.h"
+#include "split_policy.h"
 
 extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sms, attn_plan_t* out);
 
@@ -73,9 +74,26 @@ int launch_fp8(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq,
             return cuda_fail(e);
         configured = true;
     }
-    kernel<<<plan.grid, plan.threads, smem, stream>>>(tq, tk, tvt, p);
-    e = cudaGetLastError();
-    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+    // every CTA starts with item blockIdx.x: the grid never exceeds the items
+    const int grid = p.num_items < dev.num_sms ? p.num_items : dev.num_sms;
+    kernel<<<grid, plan.threads, smem, stream>>>(tq, tk, tvt, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    if (p.kv_split > 1) {
+        // the segments' merge, as a programmatic dependent launch (see attn_api.cu)
+        const int rows = p.split_units * 2 * kBr;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, attn_fwd_combine_kernel<kFp8D, CAUSAL>, p)) != cudaSuccess) return cuda_fail(e);
+    }
+    return ATTN_OK;
 }
 
 bool positive_finite(float x) { return std::isfinite(x) && x > 0.f; }
@@ -85,15 +103,38 @@ bool positive_finite(float x) { return std::isfinite(x) && x > 0.f; }
 
 using namespace elsattn;
 
-// Workspace: the transposed V codes, then a 256-byte block for the schedule counter.
+// Workspace: the transposed V codes, a 256-byte block for the schedule
+// counter, then the split units' partial O and LSE, each part 256-aligned.
 size_t vt_bytes(int B, int H, int N, int d) {
     const size_t b = static_cast<size_t>(B) * H * d * vt_pitch(N);
     return (b + 255) & ~static_cast<size_t>(255);
 }
 
+namespace {
+
+// The work schedule on the current device; no split without a usable device.
+KvSplit fp8_schedule(int B, int H, int N, int d, int causal) {
+    DeviceState* dev = nullptr;
+    attn_plan_t plan;
+    if (device_state(&dev) != ATTN_OK || attn_plan_impl(B, H, N, d, causal, dev->num_sms, &plan) != ATTN_OK)
+        return KvSplit{1, 0, 0, false};
+    return choose_kv_split(plan, dev->num_sms, B * H, N, causal);
+}
+
+}  // namespace
+
 extern "C" size_t attn_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
-    return vt_bytes(B, H, N, d) + 256;
+    size_t b = vt_bytes(B, H, N, d) + kCounterBlock;
+    if (d == kFp8D && static_cast<long long>(B) * H * N < (1ll << 31)) {
+        // the larger of the two masks' splits, so one size serves both
+        for (int causal = 0; causal < 2; ++causal) {
+            const KvSplit s = fp8_schedule(B, H, N, d, causal);
+            const size_t parts = split_part_o_bytes(s, d) + split_part_lse_bytes(s);
+            if (vt_bytes(B, H, N, d) + kCounterBlock + parts > b) b = vt_bytes(B, H, N, d) + kCounterBlock + parts;
+        }
+    }
+    return b;
 }
 
 extern "C" int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void* O, float* LSE, int B, int H, int N,
@@ -142,18 +183,22 @@ extern "C" int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void
     p.num_units = plan.num_units;
     p.heads_per_group = plan.heads_per_group;
     p.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
-    p.kv_split = 1;  // the FP8 kernel runs whole units
-    p.split_first = 0;
-    p.split_units = 0;
-    p.num_items = plan.num_units;
-    p.part_o = nullptr;
-    p.part_lse = nullptr;
-    p.sched_counter = nullptr;
     p.out_scale = v_scale;
-    // Causal units differ in length: with more of them than SMs, CTAs claim them
-    // dynamically (heaviest first) from a counter zeroed on the stream.
-    if (causal && plan.num_units > dev->num_sms) {
-        int* counter = reinterpret_cast<int*>(vt + vt_bytes(B, H, N, d));
+    // The bf16 forward's work schedule: K/V segments for launches with fewer
+    // units than SMs or a partial last wave, dynamic claiming for causal ones.
+    const KvSplit split = choose_kv_split(plan, dev->num_sms, BH, N, causal);
+    uint8_t* counter_block = vt + vt_bytes(B, H, N, d);
+    p.kv_split = split.segs;
+    p.split_first = split.first;
+    p.split_units = split.units;
+    p.num_items = plan.num_units + split.units * (split.segs - 1);
+    p.part_o = split.segs > 1 ? reinterpret_cast<float*>(counter_block + kCounterBlock) : nullptr;
+    p.part_lse =
+        split.segs > 1 ? reinterpret_cast<float*>(counter_block + kCounterBlock + split_part_o_bytes(split, d)) : nullptr;
+    p.sched_counter = nullptr;
+    if (split.dynamic) {
+        // CTAs claim items, heaviest first, from a counter zeroed on the stream
+        int* counter = reinterpret_cast<int*>(counter_block);
         cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
         if (e != cudaSuccess) return cuda_fail(e);
         p.sched_counter = counter;

@@ -92,10 +92,10 @@ struct Fp8Layout {
     static constexpr int kOFull = kODone + 2;              // [2]
     static constexpr int kOEmpty = kOFull + 2;             // [2] (128)
     static constexpr int kDrain = kOEmpty + 2;             // [2] one per MMA warp
-    static constexpr int kItemFull = kDrain + 2;           // [kItemRing] the slot holds the next unit index
+    static constexpr int kItemFull = kDrain + 2;           // [kItemRing] the slot holds the next item index
     static constexpr int kItemEmpty = kItemFull + kItemRing;  // [kItemRing] both MMA warps + 8 softmax warps read it
     static constexpr int kNumBars = kItemEmpty + kItemRing;
-    static constexpr int kFlagsOff = kBarOff + kNumBars * 8;  // tmem base slot, abort flag, unit indices
+    static constexpr int kFlagsOff = kBarOff + kNumBars * 8;  // tmem base slot, abort flag, item indices
     static constexpr int kItemOff = kFlagsOff + 8;             // [kItemRing] int
     static constexpr int kBytes = kFlagsOff + 16;
     static constexpr int kSmem = kBytes + kSmemAlign;
@@ -103,11 +103,13 @@ struct Fp8Layout {
     static_assert(2 * kSmem > 233472, "one CTA per SM: it allocates all TMEM columns");
 };
 
-// DYN: the dynamic unit schedule (p.sched_counter is set; causal launches with
-// more units than SMs): each CTA starts with unit blockIdx.x and then claims the
-// next unclaimed unit from the counter, the producer passing each claimed unit
-// to the MMA and softmax warps through a two-slot ring in shared memory (-1
-// after the last).  Without it, the static stride.
+// Work items as in the bf16 kernel (decode_item): whole units, or K/V segments
+// of the units the launch splits, whose partial results the combine kernel
+// merges.  DYN: the dynamic item schedule (p.sched_counter is set): each CTA
+// starts with item blockIdx.x and then claims the next unclaimed item from the
+// counter, the producer passing each claimed item to the MMA and softmax warps
+// through a two-slot ring in shared memory (-1 after the last).  Without it,
+// the static stride.
 template <bool CAUSAL, bool DYN = false>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -165,14 +167,16 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // a split launch's combine kernel waits for this whole grid (griddepcontrol.wait)
+    if (p.kv_split > 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kItemOff);
     // Dynamic schedule, reader side (a whole warp calls it): ring entry r is this
-    // CTA's unit r + 1, or -1 after the last; false if the wait failed.
-    auto take_item = [&](uint32_t r, int& u) -> bool {
+    // CTA's item r + 1, or -1 after the last; false if the wait failed.
+    auto take_item = [&](uint32_t r, int& w) -> bool {
         const uint32_t s = r % kItemRing;
         const bool got = __all_sync(0xffffffffu, mbar_wait(bar(L::kItemFull + s), (r / kItemRing) & 1u, ctx));
         if (!got) return false;
-        u = item_slot[s];
+        w = item_slot[s];
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::kItemEmpty + s));
         return true;
@@ -180,7 +184,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------------ TMA producer
-        // Per unit: Q_0, Q_1, then K_0, V_0^T, K_1, V_1^T, ... through the ring.
+        // Per item: Q_0, Q_1, then K_jb, V_jb^T, K_jb+1, ... through the ring.
         RingPos pos{0u, 0u};
         uint32_t issued = 0;
         uint32_t ul = 0;
@@ -188,8 +192,9 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         uint32_t q_parity = 0;  // ... and completes this phase parity of QFull[t]
         bool ok = true;
         uint32_t r = 0;  // dynamic schedule: ring entries published
-        for (int u = blockIdx.x; (DYN ? u >= 0 : u < p.num_units) && ok; ++ul) {
-            const UnitInfo ui = decode_unit<CAUSAL>(u, p);
+        for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok; ++ul) {
+            const ItemInfo item = decode_item<CAUSAL>(w, p);
+            const UnitInfo& ui = item.ui;
             q_issued = 0;
             q_parity = ul & 1u;
             for (int t = 0; t < 2 && ok; ++t) {
@@ -199,7 +204,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                 tma_load_3d(s_base + L::kQOff + t * L::kTile, &tmap_q, bar(L::kQFull + t), 0, (ui.q0 + t) * kBr, ui.bh);
                 q_issued |= 1u << t;
             }
-            for (int j = 0; j < ui.n[1] && ok; ++j) {
+            for (int j = item.jb; j < item.je && ok; ++j) {
 #pragma unroll
                 for (int kv = 0; kv < 2; ++kv) {
                     ok = mbar_wait(bar(L::kKvEmpty + pos.stage), pos.phase ^ 1u, ctx);
@@ -216,17 +221,17 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
             }
             if (!ok) break;
             if constexpr (DYN) {
-                // claim this CTA's next unit and publish it to the other roles
-                u = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
-                if (u >= p.num_units) u = -1;
+                // claim this CTA's next item and publish it to the other roles
+                w = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
+                if (w >= p.num_items) w = -1;
                 const uint32_t s = r % kItemRing;
                 if (r >= kItemRing && !(ok = mbar_wait(bar(L::kItemEmpty + s), ((r / kItemRing) - 1) & 1u, ctx)))
                     break;
-                item_slot[s] = u;
+                item_slot[s] = w;
                 mbar_arrive(bar(L::kItemFull + s));
                 ++r;
             } else {
-                u += gridDim.x;
+                w += gridDim.x;
             }
         }
         // Every issued copy lands before the CTA's shared memory is released
@@ -244,9 +249,9 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         // ------------------------------------------------------------ MMA issuers
         // Warp 1 issues tile 0's products, warp 2 tile 1's: with P in shared memory
         // the two tiles' chains are independent, and one issuing warp per tile keeps
-        // either chain from waiting on the other.  Per unit, for j = 0 .. n1: the
-        // scores S_t(j) (issued once the softmax has loaded S_t(j-1)), then
-        // O_t += P_t(j-1) V_{j-1} (half by half as P_t lands).  Both warps release
+        // either chain from waiting on the other.  Per work item, over its K/V
+        // tiles j = jb .. je: the scores S_t(j) (issued once the softmax has loaded
+        // S_t(j-1)), then O_t += P_t(j-1) V_{j-1} (half by half as P_t lands).  Both warps release
         // every K/V stage (kKvEmpty counts 2); for a K/V tile its query tile does not
         // visit (causal), the warp arrives once the stage's fill has landed, so that
         // the arrival counts toward that fill.
@@ -266,14 +271,15 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
             return __all_sync(0xffffffffu, w);
         };
         uint32_t r = 0;
-        for (int u = blockIdx.x; (DYN ? u >= 0 : u < p.num_units) && ok; ++ul) {
-            const UnitInfo ui = decode_unit<CAUSAL>(u, p);
-            const int n1 = ui.n[1], nt = ui.n[t];
+        for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok; ++ul) {
+            const ItemInfo item = decode_item<CAUSAL>(w, p);
+            // the item's K/V tiles are [jb, e1); tile t visits [jb, nt)
+            const int jb = item.jb, e1 = item.je, nt = min(item.je, item.ui.n[t]);
             ok = wait_all(bar(L::kQFull + t), ul & 1u);
             RingPos kp = kpos;                    // K_j
             RingPos vp = kpos.next(kFp8Stages);   // V_{j-1}^T
-            for (int j = 0; j <= n1 && ok; ++j) {
-                if (j < n1) {
+            for (int j = jb; j <= e1 && ok; ++j) {
+                if (j < e1) {
                     if (!(ok = wait_all(bar(L::kKvFull + kp.stage), kp.phase))) break;
                     if (j < nt) {
                         if (s_cnt > 0 && !(ok = wait_all(bar(L::kSCons + t), (s_cnt - 1) & 1u))) break;
@@ -297,7 +303,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                     }
                     kp = kp.next(kFp8Stages).next(kFp8Stages);
                 }
-                if (j == 0) continue;
+                if (j == jb) continue;
                 const int jj = j - 1;  // O_t += P_t(jj) V_jj
                 if (!(ok = wait_all(bar(L::kKvFull + vp.stage), vp.phase))) break;
                 if (jj < nt) {
@@ -305,15 +311,15 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                     const uint32_t pu = (p_cnt >> 1) & 1u;  // parity of this buffer's use
                     const uint64_t a0 = dp0 + static_cast<uint64_t>((pb * L::kTile) >> 4);
                     const uint64_t b0 = dr0 + static_cast<uint64_t>((vp.stage * L::kTile) >> 4);
-                    bool w = mbar_wait(bar(L::kPHalf + 2 * t + pb), pu, ctx);
-                    if (jj == 0) w = w && mbar_wait(bar(L::kOEmpty + t), (ul & 1u) ^ 1u, ctx);
-                    if (!(ok = __all_sync(0xffffffffu, w))) break;
+                    bool ready = mbar_wait(bar(L::kPHalf + 2 * t + pb), pu, ctx);
+                    if (jj == jb) ready = ready && mbar_wait(bar(L::kOEmpty + t), (ul & 1u) ^ 1u, ctx);
+                    if (!(ok = __all_sync(0xffffffffu, ready))) break;
                     tc_fence_after_sync();
                     if (elect_one()) {
 #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {  // keys 0-63
+                        for (int kk = 0; kk < 2; ++kk) {  // keys 0-63; the item's first product starts O_t
                             const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
-                            mma_ss_f8(t_o, a0 + off, b0 + off, idesc, (jj > 0 || kk > 0) ? 1u : 0u);
+                            mma_ss_f8(t_o, a0 + off, b0 + off, idesc, (jj > jb || kk > 0) ? 1u : 0u);
                         }
                     }
                     __syncwarp();
@@ -340,9 +346,9 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
             }
             kpos = kp;
             if constexpr (DYN) {
-                if (ok) ok = take_item(r++, u);
+                if (ok) ok = take_item(r++, w);
             } else {
-                u += gridDim.x;
+                w += gridDim.x;
             }
         }
         if (elect_one()) mma_commit(bar(L::kDrain + t));
@@ -361,14 +367,15 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         uint32_t ul = 0;
         bool ok = true;
         uint32_t r = 0;
-        for (int u = blockIdx.x; (DYN ? u >= 0 : u < p.num_units) && ok; ++ul) {
-            const UnitInfo ui = decode_unit<CAUSAL>(u, p);
+        for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok; ++ul) {
+            const ItemInfo item = decode_item<CAUSAL>(w, p);
+            const UnitInfo& ui = item.ui;
             const int qt = ui.q0 + t;
             const int qrow = qt * kBr + rloc;
-            const int nt = ui.n[t];
+            const int jb = item.jb, nt = min(item.je, ui.n[t]);  // this tile's K/V tiles are [jb, nt)
             float m_ref = -INFINITY;
             float l = 0.f;
-            for (int j = 0; j < nt; ++j, ++s_cnt) {
+            for (int j = jb; j < nt; ++j, ++s_cnt) {
                 // This iteration's P buffer is free once the O_t += P V two iterations
                 // back has read it; that also makes the product before the previous
                 // one complete, so the rescale's wait on the previous one is exact.
@@ -474,7 +481,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
                 // Rescale the O accumulator when this row's reference maximum moved
                 // (after the first half's exponentials, when their scores are dead),
                 // before the first half of P_t is released to O_t += P_t V.
-                if (__any_sync(0xffffffffu, grow && j > 0)) {
+                if (__any_sync(0xffffffffu, grow && j > jb)) {
                     // O_t must hold exactly the earlier iterations' products before the rescale
                     ok = __all_sync(0xffffffffu, mbar_wait_inline(bar(L::kODone + t), (s_cnt - 1) & 1u, ctx));
                     if (!ok) break;
@@ -507,33 +514,55 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
             const float inv_l = p.out_scale / l;
             const bool row_ok = qrow < p.N;
             const size_t grow_idx = static_cast<size_t>(ui.bh) * p.N + (row_ok ? qrow : 0);
-            uint4* orow = reinterpret_cast<uint4*>(p.O + grow_idx * D);
+            const float lse = ((m_ref == -INFINITY ? 0.f : m_ref) + lg2_approx(l)) * kLn2;
+            if (item.nseg == 1) {
+                uint4* orow = reinterpret_cast<uint4*>(p.O + grow_idx * D);
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(t_o + c, o);
-                tmem_wait_ld(o);
-                uint32_t w[16];
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c, o);
+                    tmem_wait_ld(o);
+                    uint32_t pw[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (row_ok) {
+                    for (int i = 0; i < 16; ++i)
+                        pw[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+                    if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        orow[c / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i)
+                            orow[c / 8 + i] = make_uint4(pw[4 * i], pw[4 * i + 1], pw[4 * i + 2], pw[4 * i + 3]);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
-            }
-            if (row_ok) {
-                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                p.LSE[grow_idx] = (m_use + lg2_approx(l)) * kLn2;
+                if (row_ok) p.LSE[grow_idx] = lse;
+            } else {
+                // this segment's O v_scale / l (fp32) and LSE, merged by the combine
+                // kernel (evict-last in L2: read back right after this grid)
+                const size_t pidx = (static_cast<size_t>(item.u - p.split_first) * p.kv_split + item.seg) * (2 * kBr) +
+                                    t * kBr + rloc;
+                float* orow = p.part_o + pidx * D;
+                const uint64_t keep = l2_policy_evict_last();
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c, o);
+                    tmem_wait_ld(o);
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            st_global_v4_hint(orow + c + 4 * i, __uint_as_float(o[4 * i]) * inv_l,
+                                              __uint_as_float(o[4 * i + 1]) * inv_l, __uint_as_float(o[4 * i + 2]) * inv_l,
+                                              __uint_as_float(o[4 * i + 3]) * inv_l, keep);
+                    }
+                    __syncwarp();
+                }
+                if (row_ok) st_global_hint(p.part_lse + pidx, lse, keep);
             }
             tc_fence_before_sync();
             mbar_arrive(bar(L::kOEmpty + t));
             if constexpr (DYN) {
-                ok = take_item(r++, u);
+                ok = take_item(r++, w);
             } else {
-                u += gridDim.x;
+                w += gridDim.x;
             }
         }
     }

@@ -23,12 +23,11 @@
 //
 // Work: a unit is a pair of query tiles of one (batch, head) against all the
 // K/V tiles they see.  A work item is a unit, or one segment of a unit's K/V
-// range when the launch is split (FwdParams::kv_split; the segment that
-// finishes a row last merges the row's segments).  Persistent CTAs take items
-// by a fixed stride, or claim them from a counter when the kernel is
-// instantiated with DYN (launches whose items differ in length), the producer
-// passing each claimed item to the other roles through a two-slot
-// shared-memory ring.
+// range when the launch is split (FwdParams::kv_split; a second kernel merges
+// the segments).  Persistent CTAs take items by a fixed stride, or claim them
+// from a counter when the kernel is instantiated with DYN (launches whose
+// items differ in length), the producer passing each claimed item to the
+// other roles through a two-slot shared-memory ring.
 //
 // TMEM columns: [0,128) S0 | [128,256) S1 | [256,256+d) O0 | [256+d,256+2d) O1.
 // P_t (bf16, two per column) is written over the first 64 columns of S_t once
@@ -39,12 +38,12 @@
 // Online softmax (the streaming reformulation of the IO-Aware Algorithms
 // page): per row, a reference maximum m (log2 units, scale folded in) and a
 // running sum l.  A tile whose row maximum exceeds m by more than
-// kRescaleLog2 moves m up and rescales l and the O accumulator by
+// kRescaleLog2Bf16 moves m up and rescales l and the O accumulator by
 // 2^(m_old - m_new); smaller increases keep the stale m (the terms stay below
-// 2^kRescaleLog2 and the final O / l and LSE are unchanged by the choice of
-// m).  On N(0, 1) inputs no row moves m after its first tile; on inputs with
-// rare large entries (1 % of Q and K entries times 10) a warp still rescales
-// on about 40 % of its tiles.
+// 2^kRescaleLog2Bf16 and the final O / l and LSE are unchanged by the choice
+// of m).  On N(0, 1) inputs no row moves m after its first tile; on inputs
+// with rare large entries (1 % of Q and K entries times 10) a warp rescales on
+// about 40 % of its tiles at a threshold of 8 and about 12 % at 32.
 #pragma once
 
 #include <cuda.h>
@@ -61,7 +60,7 @@
 #endif
 // Stale-maximum threshold of this kernel, log2 units (see kRescaleLog2Bf16).
 #ifndef ELS_RESCALE_LOG2_BF16
-#define ELS_RESCALE_LOG2_BF16 8
+#define ELS_RESCALE_LOG2_BF16 32
 #endif
 
 namespace elsattn {
@@ -70,7 +69,10 @@ namespace elsattn {
 // at most 2^8.
 constexpr float kRescaleLog2 = 8.0f;
 // Threshold of the bf16 kernel: terms stay at most 2^T, so l <= N 2^T and
-// |O_acc| <= N 2^T max|V| in fp32.
+// |O_acc| <= N 2^T max|V| in fp32, which at T = 32 leaves room for
+// max|V| < 2^96 / N (2^65 at N = 2^31).  A larger T moves the reference
+// maximum, and rescales O, less often on rows whose large scores arrive late
+// (about 3 % faster than T = 8 on the stress recipe, measured).
 constexpr float kRescaleLog2Bf16 = ELS_RESCALE_LOG2_BF16;
 static_assert(kRescaleLog2Bf16 >= 1.0f && kRescaleLog2Bf16 <= 64.0f, "stale-maximum threshold out of range");
 constexpr int kPolyPer32 = ELS_EXP2_POLY_PER32;
@@ -96,15 +98,13 @@ struct FwdParams {
     // kv_split segments of consecutive K/V tiles, one work item each; the other
     // units are one item each, and the items follow unit order.  A split item
     // writes O / l and its LSE to part_o / part_lse at its unit's ordinal among
-    // the split units and counts itself in part_count; the segment that counts
-    // a row last merges that row's segments (merge_split_row).
+    // the split units, and attn_fwd_combine_kernel merges the segments.
     int kv_split;          // segments per split unit (1: no split)
     int split_first;       // first split unit
     int split_units;       // units that are split (0: none)
     int num_items;         // num_units + split_units * (kv_split - 1)
     float* part_o;         // [split_units, kv_split, 2 * kBr rows of the pair, d] fp32
     float* part_lse;       // [split_units, kv_split, 2 * kBr] fp32 (natural log)
-    int* part_count = nullptr;  // [split_units, 2 * kBr]: segments of the row written so far (zero at launch)
     // Dynamic work-item schedule (kernel instantiated with DYN): each CTA starts
     // with item blockIdx.x and then claims the next unclaimed item from this
     // counter (zero at launch), so items go out in schedule order to whichever
@@ -161,7 +161,6 @@ __device__ __forceinline__ UnitInfo decode_unit(int u, const FwdParams& p) {
     return ui;
 }
 
-constexpr int kMaxKvSplit = 4;
 
 // Work item w: segment `seg` of `nseg` of a unit, covering the pair's K/V tiles
 // [jb, je); tile t visits [jb, min(je, n[t])).  The host splits a unit into s
@@ -247,68 +246,6 @@ struct SmemLayout {
     static_assert(kBytes + kSmemAlign <= smem_bytes_for(D), "shared memory layout exceeds the plan");
 };
 
-// Merge the segments of one row of a split unit: with the segments' partial
-// results (O_s = softmax over the segment's keys times V, and LSE_s),
-//     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
-// the same online-softmax combination the kernel applies across K/V tiles,
-// here across segments.  Run by the thread of the segment that finished the
-// row last, after every segment's row is visible; it writes O (bf16) and LSE,
-// then discards the row's partial O lines from L2 (nothing reads them again,
-// so they need not be written back to device memory).  Segment s of the row
-// is at part_o / part_lse index base + s 2 kBr.
-template <int D>
-__device__ __forceinline__ void merge_split_row(const float* __restrict__ part_o, const float* __restrict__ part_lse,
-                                             __nv_bfloat16* O, float* LSE, size_t base, int nseg, size_t out_row) {
-    float w[kMaxKvSplit];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) {
-        w[s] = s < nseg ? __ldcg(part_lse + base + s * (2 * kBr)) : -INFINITY;
-        mx = fmaxf(mx, w[s]);
-    }
-    float wsum = 0.f;
-#pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) {
-        w[s] = s < nseg ? expf(w[s] - mx) : 0.f;
-        wsum += w[s];
-    }
-    const float inv = 1.f / wsum;
-#pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) w[s] *= inv;
-    uint4* dst = reinterpret_cast<uint4*>(O + out_row * D);
-#pragma unroll 2
-    for (int c = 0; c < D; c += 8) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int s = 0; s < kMaxKvSplit; ++s) {
-            if (s < nseg) {
-                const float4* src = reinterpret_cast<const float4*>(part_o + (base + s * (2 * kBr)) * D + c);
-                const float4 a = __ldcg(src), b = __ldcg(src + 1);
-                acc[0] = fmaf(w[s], a.x, acc[0]);
-                acc[1] = fmaf(w[s], a.y, acc[1]);
-                acc[2] = fmaf(w[s], a.z, acc[2]);
-                acc[3] = fmaf(w[s], a.w, acc[3]);
-                acc[4] = fmaf(w[s], b.x, acc[4]);
-                acc[5] = fmaf(w[s], b.y, acc[5]);
-                acc[6] = fmaf(w[s], b.z, acc[6]);
-                acc[7] = fmaf(w[s], b.w, acc[7]);
-            }
-        }
-        dst[c / 8] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                                pack_bf16x2(acc[6], acc[7]));
-    }
-    LSE[out_row] = mx + logf(wsum);
-    // every value read above has been consumed by the stores: drop the lines
-#pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) {
-        if (s < nseg) {
-            const float* row = part_o + (base + s * (2 * kBr)) * D;
-#pragma unroll
-            for (int b = 0; b < D * 4; b += 128) l2_discard_line(reinterpret_cast<const char*>(row) + b);
-        }
-    }
-}
-
 // DYN: the dynamic work-item schedule (p.sched_counter is set); without it the
 // static schedule is compiled with no trace of the item ring.
 template <int D, bool CAUSAL, bool DYN = false>
@@ -361,6 +298,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // A split launch's combine kernel may be scheduled onto SMs as this grid's
+    // CTAs retire; it waits for this whole grid (griddepcontrol.wait) before it
+    // reads the partial results.
+    if (p.kv_split > 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kItemOff);
     // Every role starts with item blockIdx.x (the grid never exceeds the item
     // count).  The static schedule then advances by gridDim.x; the dynamic one
@@ -722,13 +663,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
                 if (row_ok) p.LSE[grow_idx] = lse;
             } else {
-                // This segment's O / l (fp32) and LSE go to the workspace; the
-                // segment that counts the row last merges the row's segments.
-                const int ord = item.u - p.split_first;  // the unit's place among the split units
-                const int rr = t * kBr + rloc;           // row within the pair
-                const size_t base = static_cast<size_t>(ord) * p.kv_split * (2 * kBr) + rr;  // segment s at base + s 2 kBr
-                const size_t pidx = base + static_cast<size_t>(item.seg) * (2 * kBr);
-                float4* orow = reinterpret_cast<float4*>(p.part_o + pidx * D);
+                // This segment's O / l (fp32) and LSE, merged by the combine
+                // kernel.  Stored with an evict-last L2 policy: they are read
+                // back right after this grid, and the combine kernel drops them
+                // from L2 after reading, so they need not reach device memory.
+                const size_t pidx = (static_cast<size_t>(item.u - p.split_first) * p.kv_split + item.seg) * (2 * kBr) +
+                                    t * kBr + rloc;
+                float* orow = p.part_o + pidx * D;
+                const uint64_t keep = l2_policy_evict_last();
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
                     uint32_t o[32];
@@ -737,20 +679,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     if (row_ok) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            orow[c / 4 + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                                          __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+                            st_global_v4_hint(orow + c + 4 * i, __uint_as_float(o[4 * i]) * inv_l,
+                                              __uint_as_float(o[4 * i + 1]) * inv_l, __uint_as_float(o[4 * i + 2]) * inv_l,
+                                              __uint_as_float(o[4 * i + 3]) * inv_l, keep);
                     }
                 }
-                if (row_ok) {
-                    p.part_lse[pidx] = lse;
-                    // release this row's partial result, then count it; the
-                    // thread that counts last sees every segment's writes
-                    __threadfence();
-                    if (atomicAdd(p.part_count + static_cast<size_t>(ord) * (2 * kBr) + rr, 1) == item.nseg - 1) {
-                        __threadfence();
-                        merge_split_row<D>(p.part_o, p.part_lse, p.O, p.LSE, base, item.nseg, grow_idx);
-                    }
-                }
+                if (row_ok) st_global_hint(p.part_lse + pidx, lse, keep);
             }
             tc_fence_before_sync();
             mbar_arrive(bar(L::kOEmpty + t));
@@ -768,6 +702,72 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Merge the segments of the split units: per row, with the segments' partial
+// results (O_s = softmax over the segment's keys times V, LSE_s),
+//     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
+// the same online-softmax combination as inside the kernel, across segments,
+// in the fixed segment order.  One warp per row of the split units (2 kBr rows
+// each; lane l holds columns [kPer l, kPer l + kPer), so every partial row is
+// one coalesced read); the rows of the other units were written by the
+// attention kernel itself.  After the merged row is written, its partial O
+// lines are discarded from L2: nothing reads them again, so they are not
+// written back to device memory.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256) attn_fwd_combine_kernel(const FwdParams p) {
+    constexpr int kPer = D / 32;                 // columns per lane
+    constexpr int kLinesPerRow = D * 4 / 128;   // 128-byte lines of one partial row
+    // launched as a programmatic dependent of the attention kernel: wait until
+    // that grid has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int prow = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);  // over split_units * 2 kBr
+    const int lane = threadIdx.x & 31;
+    if (prow >= p.split_units * 2 * kBr) return;
+    const int ord = prow / (2 * kBr);
+    const int rr = prow - ord * 2 * kBr;  // row within the pair: tile rr / kBr, row rr % kBr
+    const UnitInfo ui = decode_unit<CAUSAL>(p.split_first + ord, p);
+    const int qrow = ui.q0 * kBr + rr;
+    if (qrow >= p.N) return;
+    const size_t row = static_cast<size_t>(ui.bh) * p.N + qrow;
+    const int nseg = p.kv_split;
+    const size_t base = static_cast<size_t>(ord) * nseg * (2 * kBr) + rr;  // segment s at base + s * 2 kBr
+    float w[kMaxKvSplit];
+    float x[kMaxKvSplit][kPer];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) {
+        w[s] = s < nseg ? __ldcg(p.part_lse + base + s * (2 * kBr)) : -INFINITY;
+        mx = fmaxf(mx, w[s]);
+        const float* src = p.part_o + (base + s * (2 * kBr)) * D + lane * kPer;
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) x[s][c] = s < nseg ? __ldcg(src + c) : 0.f;
+    }
+    float wsum = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) {
+        w[s] = s < nseg ? expf(w[s] - mx) : 0.f;  // now the segment weights
+        wsum += w[s];
+    }
+    const float inv = 1.f / wsum;
+    float acc[kPer];
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxKvSplit; ++s) {
+        const float ws = w[s] * inv;
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) acc[c] = fmaf(ws, x[s][c], acc[c]);
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(p.O + row * D + lane * kPer);
+#pragma unroll
+    for (int c = 0; c < kPer; c += 2) dst[c / 2] = pack_bf16x2(acc[c], acc[c + 1]);
+    if (lane == 0) p.LSE[row] = mx + logf(wsum);
+    // every value read above has been consumed by the stores: drop the lines
+    if (lane < nseg * kLinesPerRow) {
+        const int s = lane / kLinesPerRow, part = lane - s * kLinesPerRow;
+        l2_discard_line(reinterpret_cast<const char*>(p.part_o + (base + s * (2 * kBr)) * D) + part * 128);
     }
 }
 

@@ -20,6 +20,7 @@ constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per CTA on s
 constexpr int kSmemAlign = 1024;    // slack to align the tiles to the 1024-byte swizzle atom
 constexpr int kFixedBarriers = 19;  // mbarriers besides the two per K/V stage
 constexpr int kFlagBytes = 16;      // TMEM base address slot, abort flag, two work-item slots
+constexpr int kMaxKvSplit = 4;      // most K/V segments a unit is cut into
 
 // Bytes of one [128 x d] tile of `esize`-byte elements (Q, K and V tiles all
 // have this size since kBr == kBc): bf16 (esize 2) by default, E4M3 (esize 1)

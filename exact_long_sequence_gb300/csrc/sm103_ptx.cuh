@@ -291,6 +291,24 @@ __device__ __forceinline__ void tmem_wait_st() {
 #undef ELS_U8
 #undef ELS_I8
 
+// An L2 cache policy that keeps the lines it is attached to over others
+// (evict last), for data that is read back soon.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Global stores carrying an L2 cache policy.
+__device__ __forceinline__ void st_global_v4_hint(float* p, float a, float b, float c, float d, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d),
+                 "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void st_global_hint(float* p, float a, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(a), "l"(pol) : "memory");
+}
+
 // Invalidate one 128-byte line of global memory in L2 without writing it back
 // (its contents become undefined): for scratch data that nothing reads again.
 __device__ __forceinline__ void l2_discard_line(const void* line128) {

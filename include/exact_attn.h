@@ -129,15 +129,15 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
  *     outputs are bit-identical to it.
  * A segment is a work item of its own: it writes its partial result (O over
  * the segment's keys, normalised, fp32, and that segment's LSE) to `workspace`
- * and counts itself in a per-row counter there; the segment that counts a row
- * last merges the row's segments, in the same kernel, by
+ * (with an L2 evict-last policy), and a second kernel on `stream` merges the
+ * segments of each row by
  *     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
  * the combination step of the online softmax (the streaming reformulation of
- * the IO-Aware Algorithms page) applied across segments, and then drops the
+ * the IO-Aware Algorithms page) applied across segments, then drops the
  * partial rows from L2 without writing them back.  The result is the same
- * operation as attn_fwd, up to floating-point rounding.  The call zeroes the
- * schedule counter and the per-row counters with a memset on `stream` before
- * the kernel: one memset and one kernel launch.
+ * operation as attn_fwd, up to floating-point rounding.  Launches on `stream`:
+ * a 4-byte memset of the schedule counter (dynamic schedule only), the
+ * attention kernel, and the combine kernel (split launches only).
  *   arguments as attn_fwd, plus
  *   workspace       : device buffer of at least attn_fwd_split_workspace_bytes()
  *                     bytes, 16-byte aligned, owned by the caller, not used by

@@ -16,8 +16,12 @@ pass a saturation bug, and a planted case whose terms reach 2^8, the largest
 the stale-maximum threshold allows, with V at E4M3's largest magnitudes.  A
 one-hot attention case (every query attends to one key with weight 1, which
 E4M3 holds exactly) pins the layout of P and of the transposed V to the exact
-answer.
+answer.  Launches with fewer units than SMs, or a partial last wave, are cut
+into K/V segments as in the bf16 forward and merged by the same combine
+kernel; their cases are held to the same bound.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -116,6 +120,30 @@ def test_fp8_terms_at_the_threshold_with_v_at_the_ceiling(oracle_mod):
     V codes are E4M3's largest magnitudes.  A kernel whose terms saturated would break the bound."""
     q8, k8, v8, sc, scale = near_ceiling_inputs()
     check(oracle_mod, q8, k8, v8, sc, False, label="near the E4M3 ceiling", scale=scale)
+
+
+@pytest.mark.parametrize("B,H,N,causal", [(1, 1, 4096, False), (1, 1, 8192, True), (3, 1, 7000, True),
+                                           (1, 13, 3000, False)])
+def test_fp8_split_launches(oracle_mod, B, H, N, causal):
+    """Launches that take the bf16 forward's work schedule with K/V segments: 16 units cut into
+    four, a causal mask with the heaviest units cut, a ragged causal shape whose segments are
+    claimed dynamically, and a partial last wave (156 units).  The combine kernel merges the
+    segments; every row's result must meet the same per-term bound, and a second launch into
+    fresh outputs must give the same bits."""
+    lib = ela.load_library()
+    segs = [ctypes.c_int() for _ in range(4)]
+    assert lib.attn_fwd_split_choice(B, H, N, D, int(causal), torch.cuda.get_device_properties(0).multi_processor_count,
+                                     *[ctypes.byref(x) for x in segs]) == ela.ATTN_OK
+    assert segs[0].value > 1, "this shape is meant to split"
+    q8, k8, v8, sc = workloads.make_inputs_fp8(B, H, N, D, seed=640 + N)
+    rows = workloads.sample_rows(B * H, N, 62, seed=N)
+    rows = torch.cat([torch.tensor([[0, N - 1]]).repeat(B * H, 1), rows], dim=1).sort(dim=1).values
+    check(oracle_mod, q8, k8, v8, sc, causal, rows=rows.numpy(), label=f"split B={B} H={H} N={N} causal={causal}")
+    a = ela.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), sc, causal=causal)
+    b = ela.attn_fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), sc, causal=causal,
+                         out=torch.full((B, H, N, D), float("nan"), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
 def test_fp8_rejects_bad_arguments():

@@ -3,7 +3,8 @@
 The kernel (csrc/attn_fwd_kernel.cuh) streams each query row's keys in tiles
 of 128 and keeps, per row, a reference maximum m in log2 units (the scale
 folded in). It moves m only when a tile's maximum exceeds it by more than
-2^T (T = 8), rescaling l and the O accumulator by 2^(m_old - m_new). Every
+T (T = 32 in the bf16 kernel, 8 in the FP8 one, whose P is E4M3), rescaling l
+and the O accumulator by 2^(m_old - m_new). Every
 other tile's terms P = 2^(c s - m) are taken against the stale m and stay
 below 2^T. P is summed into l in fp32, rounded to bf16 for O += P V (fp32
 accumulation), and the row ends with O / l in bf16 and LSE = ln 2 (m + log2 l).
@@ -15,8 +16,8 @@ The claim that makes the lazy reference exact is that O / l and LSE do not
 depend on which m is used, up to rounding. This test replays the arithmetic in
 fp32 and bf16 on sampled rows of the seeded workloads, the spiky one among
 them, where the reference does move mid-row. It checks:
-- the result is within the parity tolerances of the oracle, at T = 8 and at
-  larger T;
+- the result is within the parity tolerances of the oracle, at T = 8, 32
+  and 64;
 - results for different T differ only by rounding;
 - no term exceeds 2^T.
 The model is not the kernel, whose own parity tests run on the GPU. It checks

@@ -1,17 +1,16 @@
 """GPU parity of the K/V split (attn_fwd_split).
 
 Problems with fewer work units than SMs cut the K/V range of their long units
-into segments that run on different CTAs; the segment that finishes a row last
-merges the row's partial results by their LSE weights, in the kernel.  Causal
-problems may take the dynamic schedule for their segments.  The result is the
-same operation as attn_fwd, so the forward's tolerances apply unchanged: against
-the fp64 oracle max |dO| <= 2e-2 and per-row |dLSE| <= 1e-3 |LSE|.  The shapes
-below are chosen so that the launch splits units into 2, 3 and 4 segments on a
-152-SM GB300 (the test checks the split the library reports is the expected
-one), with causal masks, ragged lengths, several schedule groups, units left
-whole beside split ones, and split items claimed dynamically.  A second launch
-into fresh outputs with the same workspace must give the same bits (the
-per-row segment counts start from zero on every launch).
+into segments that run on different CTAs; a second kernel merges the segments'
+partial results of each row by their LSE weights.  Causal problems may take the
+dynamic schedule for their segments.  The result is the same operation as
+attn_fwd, so the forward's tolerances apply unchanged: against the fp64 oracle
+max |dO| <= 2e-2 and per-row |dLSE| <= 1e-3 |LSE|.  The shapes below are chosen
+so that the launch splits units into 2, 3 and 4 segments on a 152-SM GB300 (the
+test checks the split the library reports is the expected one), with causal
+masks, ragged lengths, several schedule groups, units left whole beside split
+ones, and split items claimed dynamically.  A second launch into fresh outputs
+with the same workspace must give the same bits.
 
 Causal problems with more units than SMs take the same entry's dynamic
 schedule instead: CTAs claim units from a counter in the workspace.  Each unit
@@ -48,7 +47,8 @@ def chosen_split(B, H, N, d, causal):
 # With more (equal, non-causal) units, the units of the last partial wave are.
 CASES = [
     (1, 8, 4096, 64, True, 2),     # the causal d = 64 workload: 128 units, 120 halved, claimed dynamically
-    (1, 4, 6000, 128, True, 3),    # ragged causal, 84 of 96 units in thirds, claimed dynamically
+    (1, 4, 6000, 128, True, 2),    # ragged causal, 96 units: the 56 heaviest halved in one wave
+    (3, 1, 7000, 128, True, 3),    # ragged causal, three schedule groups, 72 units in thirds, dynamic
     (3, 1, 7000, 64, True, 3),     # ragged causal, three schedule groups, dynamic
     (1, 2, 8192, 128, False, 2),   # 64 equal units, all split
     (1, 1, 1000, 64, False, 3),    # 4 units of 8 K/V tiles, ragged length

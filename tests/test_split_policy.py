@@ -59,6 +59,7 @@ def unit_tiles(u, BH, N, causal, G):
 PINNED = {
     (1, 1, 256, 64, False): (1, 0, 0, 0),        # C1: one unit of two K/V tiles
     (1, 8, 4096, 64, True): (2, 0, 120, 1),      # C2: 120 of 128 units halved, 248 items claimed dynamically
+                                                 # (45.9 -> 42.6 us against the static one-wave split)
     (1, 16, 16384, 128, False): (4, 912, 112, 0),  # C3: the last partial wave (1024 = 6 * 152 + 112)
     (1, 8, 65536, 128, True): (1, 0, 0, 1),      # C4: dynamic schedule
     (4, 32, 8192, 128, True): (1, 0, 0, 1),      # C5: dynamic schedule
@@ -72,6 +73,9 @@ PINNED = {
     (1, 1, 4096, 64, False): (4, 0, 16, 0),      # 47.7 -> 23.2 us
     (1, 1, 4096, 64, True): (3, 0, 13, 0),       # 47.8 -> 27.3 us
     (1, 1, 8192, 64, True): (4, 0, 26, 0),       # 86.7 -> 35.5 us
+    # dynamic splits where the estimate beats the best static one by the margin
+    (3, 1, 7000, 64, True): (3, 0, 72, 1),       # static 49.9 -> dynamic 46.1 us
+    (1, 4, 6000, 128, True): (2, 0, 56, 0),      # the dynamic estimate is not enough better: static
 }
 
 
