@@ -54,13 +54,14 @@ BWD_FLOP_FACTOR = 2.5
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "sm103_ptx.cuh", "plan.h", "plan.cpp", "attn_api.cu"]
+KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "sm103_ptx.cuh", "exp2_poly.h", "plan.h", "plan.cpp", "split_policy.cpp",
+                  "attn_api.cu"]
 # The sources each pass's recorded traffic depends on: an entry of the traffic file is used only
 # while their hash is the one it was captured with.
 PASS_SOURCES = {
     "fwd": KERNEL_SOURCES,
-    "fp8": ["attn_fwd_fp8_kernel.cuh", "attn_fwd_kernel.cuh", "sm103_ptx.cuh", "plan.h", "plan.cpp",
-            "attn_fp8_api.cu"],
+    "fp8": ["attn_fwd_fp8_kernel.cuh", "attn_fwd_kernel.cuh", "sm103_ptx.cuh", "exp2_poly.h", "plan.h", "plan.cpp",
+            "split_policy.cpp", "attn_fp8_api.cu"],
     "bwd": ["attn_bwd_kernel.cuh", "sm103_ptx.cuh", "sm103_bulk.cuh", "plan.h", "attn_bwd_api.cu"],
     "rows": ["rowwise_kernels.cuh", "rowwise_api.cu"],
 }
@@ -387,6 +388,8 @@ def run_gb300_fp8(args, w):
         return 0
     peak_bf16, peak_bf16_sustained, peak_kind = read_peaks()
     peak = 2.0 * peak_bf16
+    # the V transpose and the attention kernel, plus the combine kernel of a K/V split
+    fp8_launches = 3 if ela.split_segments(w.B, w.H, w.N, w.d, w.causal) > 1 else 2
     kernel_ms = statistics.mean(step_ms)
     achieved = w.flops / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
@@ -394,7 +397,8 @@ def run_gb300_fp8(args, w):
                               "tensor ratio (4.5 / 2.25 PFLOP/s)"),
                 "traffic": recorded_traffic("fp8:" + w.name, "fp8"), "algorithmic_flops_per_launch": w.flops,
                 "kernel_ms": kernel_ms,
-                "note": "step = the V transpose and the attention kernel; the step time is used for both",
+                "note": ("step = the V transpose, the attention kernel and, for a K/V split, the combine kernel; "
+                         "the step time is used for all"),
                 "frac_of_bf16_peak": achieved / peak_bf16}
     if peak_bf16_sustained:
         roofline["frac_of_sustained"] = achieved / (2.0 * peak_bf16_sustained)
@@ -403,7 +407,7 @@ def run_gb300_fp8(args, w):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": slowest * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
         "config": workload_config(w, f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"),
-        "roofline": roofline, "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),
+        "roofline": roofline, "gpu_launches": fp8_launches * args.steps, "clocks": clocks.summary(),
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
         "e2e": None,
     }
@@ -663,12 +667,12 @@ def run_gb300(args, w):
     lse = torch.empty(shape[:3], dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     # Workloads with fewer work units than SMs, or a partial last wave, take the K/V split (the
-    # segment that finishes a row last merges it in the kernel); causal workloads with more units
-    # than SMs take the dynamic schedule.  Both use a workspace allocated once, outside the timed
-    # region, whose counters a memset on the stream zeroes before each launch.
+    # attention kernel and the combine kernel); causal workloads take the dynamic schedule (a
+    # counter zeroed by a 4-byte memset on the stream before each launch).  The workspace is
+    # allocated once, outside the timed region.
     split_bytes = ela.split_workspace_bytes(w.B, w.H, w.N, w.d, w.causal)
     split_ws = torch.empty(split_bytes, dtype=torch.uint8, device=dev) if split_bytes else None
-    launches_per_step = 1
+    launches_per_step = 2 if ela.split_segments(w.B, w.H, w.N, w.d, w.causal) > 1 else 1
 
     for _ in range(max(3, args.warmup)):
         ela.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream, workspace=split_ws)
@@ -741,9 +745,9 @@ def run_gb300(args, w):
                 "traffic": recorded_traffic(w.name),
                 "algorithmic_flops_per_launch": w.flops, "kernel_ms": kernel_ms,
                 "io_bound_bytes": w.io_bytes}
-    if split_bytes:
-        roofline["note"] = ("the step is the counters' memset and the attention kernel; "
-                            "the step time is used for the kernel")
+    if launches_per_step == 2:
+        roofline["note"] = ("K/V split: the step is the attention kernel plus the combine kernel (about 1 % of "
+                            "it); the step time is used for both")
     if peak_sustained:
         roofline["frac_of_sustained"] = achieved / peak_sustained
     line = {

@@ -21,7 +21,7 @@ struct DeviceState {
     uint32_t* error_word = nullptr;  // 256-byte device block, first word = error code
     bool smem_configured[2][2][2] = {};                                   // forward <d == 128><causal><dynamic schedule>
     bool bwd_smem_configured[2][2] = {{false, false}, {false, false}};  // backward <d == 128><causal>
-    bool fp8_smem_configured[2][2] = {};                                  // FP8 forward <causal><dynamic schedule>
+    bool fp8_smem_configured[2][2][2] = {};  // FP8 forward <causal><dynamic schedule><K/V segments>
 };
 
 // The cudaError_t of this thread's most recent ATTN_ERR_CUDA.

@@ -232,12 +232,13 @@ namespace {
 // Streams and events of the host-buffer entry point, one set per device,
 // created on first use.  Copies in, kernels and copies out of consecutive
 // chunks of (batch, head) pairs run on separate streams so that the transfers
-// overlap the computation; two compute streams let one chunk's kernel start on
-// the SMs the previous chunk's kernel has finished with.
+// overlap the computation; rotating compute streams let one chunk's kernel
+// start on the SMs the previous chunk's kernel has finished with.
 constexpr int kMaxChunks = 8;
+constexpr int kCompStreams = 3;
 struct HostPipe {
     bool ready = false;
-    cudaStream_t h2d = nullptr, d2h = nullptr, comp[2] = {nullptr, nullptr};
+    cudaStream_t h2d = nullptr, d2h = nullptr, comp[kCompStreams] = {};
     cudaEvent_t start = nullptr, done = nullptr, in[kMaxChunks] = {}, out[kMaxChunks] = {};
 };
 std::mutex g_pipe_mutex;
@@ -251,10 +252,10 @@ int host_pipe(HostPipe** out) {
     HostPipe& hp = g_pipe[dev];
     if (!hp.ready) {
         const unsigned f = cudaStreamNonBlocking;
+        for (int c = 0; c < kCompStreams; ++c)
+            if ((e = cudaStreamCreateWithFlags(&hp.comp[c], f)) != cudaSuccess) return cuda_fail(e);
         if ((e = cudaStreamCreateWithFlags(&hp.h2d, f)) != cudaSuccess ||
             (e = cudaStreamCreateWithFlags(&hp.d2h, f)) != cudaSuccess ||
-            (e = cudaStreamCreateWithFlags(&hp.comp[0], f)) != cudaSuccess ||
-            (e = cudaStreamCreateWithFlags(&hp.comp[1], f)) != cudaSuccess ||
             (e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) != cudaSuccess ||
             (e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming)) != cudaSuccess)
             return cuda_fail(e);
@@ -304,23 +305,41 @@ extern "C" int attn_fwd_host(const void* Qh, const void* Kh, const void* Vh, voi
         (e = cudaStreamWaitEvent(hp->h2d, hp->start, 0)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(hp->d2h, hp->start, 0)) != cudaSuccess)
         return cuda_fail(e);
+    // 1. every chunk's copies in, back to back: the two directions share the
+    //    host link, and interleaved with the copies out each ran at about two
+    //    thirds of its rate alone
     int c = 0;
     for (int h0 = 0; h0 < BH; h0 += per, ++c) {
         const int hn = (BH - h0) < per ? (BH - h0) : per;
         const size_t off = static_cast<size_t>(h0) * head_bytes, len = static_cast<size_t>(hn) * head_bytes;
-        const size_t loff = static_cast<size_t>(h0) * head_lse;
-        cudaStream_t comp = hp->comp[c & 1];
         if ((e = cudaMemcpyAsync(q + off, qh + off, len, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
             (e = cudaMemcpyAsync(k + off, kh + off, len, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
             (e = cudaMemcpyAsync(v + off, vh + off, len, cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess ||
-            (e = cudaEventRecord(hp->in[c], hp->h2d)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(comp, hp->in[c], 0)) != cudaSuccess)
+            (e = cudaEventRecord(hp->in[c], hp->h2d)) != cudaSuccess)
             return cuda_fail(e);
+    }
+    // 2. each chunk's kernel once its inputs are in, on rotating compute streams
+    //    so that a chunk's kernel can take the SMs the previous one leaves idle
+    c = 0;
+    for (int h0 = 0; h0 < BH; h0 += per, ++c) {
+        const int hn = (BH - h0) < per ? (BH - h0) : per;
+        const size_t off = static_cast<size_t>(h0) * head_bytes;
+        const size_t loff = static_cast<size_t>(h0) * head_lse;
+        cudaStream_t comp = hp->comp[c % kCompStreams];
+        if ((e = cudaStreamWaitEvent(comp, hp->in[c], 0)) != cudaSuccess) return cuda_fail(e);
         if ((st = attn_fwd(q + off, k + off, v + off, o + off, lse + loff, 1, hn, N, d, causal, scale, comp)) !=
             ATTN_OK)
             return st;
-        if ((e = cudaEventRecord(hp->out[c], comp)) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(hp->d2h, hp->out[c], 0)) != cudaSuccess ||
+        if ((e = cudaEventRecord(hp->out[c], comp)) != cudaSuccess) return cuda_fail(e);
+    }
+    // 3. the copies out, once every copy in has landed, each after its chunk's kernel
+    if ((e = cudaStreamWaitEvent(hp->d2h, hp->in[c - 1], 0)) != cudaSuccess) return cuda_fail(e);
+    c = 0;
+    for (int h0 = 0; h0 < BH; h0 += per, ++c) {
+        const int hn = (BH - h0) < per ? (BH - h0) : per;
+        const size_t off = static_cast<size_t>(h0) * head_bytes, len = static_cast<size_t>(hn) * head_bytes;
+        const size_t loff = static_cast<size_t>(h0) * head_lse;
+        if ((e = cudaStreamWaitEvent(hp->d2h, hp->out[c], 0)) != cudaSuccess ||
             (e = cudaMemcpyAsync(oh + off, o + off, len, cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess ||
             (e = cudaMemcpyAsync(LSEh + loff, lse + loff, static_cast<size_t>(hn) * head_lse * 4,
                                  cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess)

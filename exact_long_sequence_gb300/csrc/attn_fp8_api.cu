@@ -58,16 +58,20 @@ __global__ void __launch_bounds__(256) transpose_v_e4m3(const uint8_t* V, uint8_
     }
 }
 
-template <bool CAUSAL, bool DYN = false>
+template <bool CAUSAL, bool DYN = false, bool SPLIT = false>
 int launch_fp8(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, const CUtensorMap& tk,
                const CUtensorMap& tvt, const FwdParams& p, cudaStream_t stream) {
+    if constexpr (!SPLIT) {
+        // split launches take the instantiation with K/V segments
+        if (p.kv_split > 1) return launch_fp8<CAUSAL, DYN, true>(dev, plan, tq, tk, tvt, p, stream);
+    }
     if constexpr (CAUSAL && !DYN) {
         // causal launches with a schedule counter take the dynamic instantiation
-        if (p.sched_counter != nullptr) return launch_fp8<CAUSAL, true>(dev, plan, tq, tk, tvt, p, stream);
+        if (p.sched_counter != nullptr) return launch_fp8<CAUSAL, true, SPLIT>(dev, plan, tq, tk, tvt, p, stream);
     }
-    auto kernel = attn_fwd_fp8_kernel<CAUSAL, DYN>;
+    auto kernel = attn_fwd_fp8_kernel<CAUSAL, DYN, SPLIT>;
     constexpr int smem = Fp8Layout::kSmem;
-    bool& configured = dev.fp8_smem_configured[CAUSAL][DYN];
+    bool& configured = dev.fp8_smem_configured[CAUSAL][DYN][SPLIT];
     cudaError_t e;
     if (!configured) {
         if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)

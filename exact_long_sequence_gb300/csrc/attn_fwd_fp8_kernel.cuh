@@ -110,7 +110,25 @@ struct Fp8Layout {
 // counter, the producer passing each claimed item to the MMA and softmax warps
 // through a two-slot ring in shared memory (-1 after the last).  Without it,
 // the static stride.
-template <bool CAUSAL, bool DYN = false>
+// A work item: with SPLIT, decode_item's unit or K/V segment; without it the
+// whole unit w (the instantiation that unsplit launches run).
+template <bool CAUSAL, bool SPLIT>
+__device__ __forceinline__ ItemInfo fp8_item(int w, const FwdParams& p) {
+    if constexpr (SPLIT) {
+        return decode_item<CAUSAL>(w, p);
+    } else {
+        ItemInfo it;
+        it.ui = decode_unit<CAUSAL>(w, p);
+        it.u = w;
+        it.seg = 0;
+        it.nseg = 1;
+        it.jb = 0;
+        it.je = it.ui.n[1];
+        return it;
+    }
+}
+
+template <bool CAUSAL, bool DYN = false, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_vt, const FwdParams p) {
@@ -168,7 +186,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     // a split launch's combine kernel waits for this whole grid (griddepcontrol.wait)
-    if (p.kv_split > 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     volatile int* item_slot = reinterpret_cast<volatile int*>(smem + L::kItemOff);
     // Dynamic schedule, reader side (a whole warp calls it): ring entry r is this
     // CTA's item r + 1, or -1 after the last; false if the wait failed.
@@ -193,7 +211,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         bool ok = true;
         uint32_t r = 0;  // dynamic schedule: ring entries published
         for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok; ++ul) {
-            const ItemInfo item = decode_item<CAUSAL>(w, p);
+            const ItemInfo item = fp8_item<CAUSAL, SPLIT>(w, p);
             const UnitInfo& ui = item.ui;
             q_issued = 0;
             q_parity = ul & 1u;
@@ -272,7 +290,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         };
         uint32_t r = 0;
         for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok; ++ul) {
-            const ItemInfo item = decode_item<CAUSAL>(w, p);
+            const ItemInfo item = fp8_item<CAUSAL, SPLIT>(w, p);
             // the item's K/V tiles are [jb, e1); tile t visits [jb, nt)
             const int jb = item.jb, e1 = item.je, nt = min(item.je, item.ui.n[t]);
             ok = wait_all(bar(L::kQFull + t), ul & 1u);
@@ -368,7 +386,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
         bool ok = true;
         uint32_t r = 0;
         for (int w = blockIdx.x; (DYN ? w >= 0 : w < p.num_items) && ok; ++ul) {
-            const ItemInfo item = decode_item<CAUSAL>(w, p);
+            const ItemInfo item = fp8_item<CAUSAL, SPLIT>(w, p);
             const UnitInfo& ui = item.ui;
             const int qt = ui.q0 + t;
             const int qrow = qt * kBr + rloc;
@@ -515,7 +533,7 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
             const bool row_ok = qrow < p.N;
             const size_t grow_idx = static_cast<size_t>(ui.bh) * p.N + (row_ok ? qrow : 0);
             const float lse = ((m_ref == -INFINITY ? 0.f : m_ref) + lg2_approx(l)) * kLn2;
-            if (item.nseg == 1) {
+            if (!SPLIT || item.nseg == 1) {
                 uint4* orow = reinterpret_cast<uint4*>(p.O + grow_idx * D);
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {

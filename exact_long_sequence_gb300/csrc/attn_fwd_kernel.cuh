@@ -511,7 +511,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const int qt = ui.q0 + t;
             const int qrow = qt * kBr + rloc;
             const int jb = item.jb;
-            const int et = min(item.je, ui.n[t]);  // this tile's K/V tiles are [jb, et)
+            const int et = min(item.je, t == 0 ? ui.n[0] : ui.n[1]);  // this tile's K/V tiles are [jb, et)
             float m_ref = -INFINITY;
             float l = 0.f;
             for (int j = jb; j < et; ++j) {

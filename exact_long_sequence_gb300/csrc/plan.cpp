@@ -35,8 +35,11 @@
 // Device-memory traffic: each (batch, head)'s K and V come from HBM once when
 // the K/V of the heads streamed at the same time fit in the L2 budget (the
 // head-major order keeps the CTAs in flight on few heads; the causal order
-// runs heads in groups sized to that budget); beyond it, the share of the
-// re-reads that no longer hits L2 is charged to HBM as well.
+// runs heads in groups sized to that budget); beyond it, every wave of a
+// head's units after the first re-reads the share that L2 no longer holds.
+// Against ncu DRAM counts on a GB300 the estimate is within about 30 %: the
+// headline workload 270 MB (measured 276), B1 H8 N65536 causal 539 MB (reads
+// 589), one causal head of 262144 keys 460 MB (reads 547).
 #include <cmath>
 
 #include "../../include/exact_attn.h"
@@ -140,21 +143,20 @@ extern "C" int attn_plan_impl(int B, int H, int N, int d, int causal, int num_sm
 
     // Heads whose K/V are streamed at the same time.  Non-causal, head-major:
     // the grid's CTAs cover `grid` consecutive units, which span at most
-    // ceil(grid / pairs) + 1 heads.  Causal: one group of heads at a time (a
-    // group's K/V take half of the budget, which leaves room for the next
-    // group's heaviest units starting while the current group ends).
-    long long heads_in_flight;
-    if (!causal) {
-        heads_in_flight = (out->grid + pairs - 1) / pairs + 1;
-    } else {
-        heads_in_flight = g;
-    }
+    // ceil(grid / pairs) + 1 heads.  Causal: one group of heads, and the first
+    // head of the next group, whose heaviest units start while the current
+    // group's lightest ones end.
+    long long heads_in_flight = causal ? g + 1 : (out->grid + pairs - 1) / pairs + 1;
     if (heads_in_flight > BH) heads_in_flight = BH;
     out->kv_in_flight_bytes = static_cast<double>(heads_in_flight) * kv_head_bytes;
     out->l2_fit = out->kv_in_flight_bytes <= kL2KvBudget ? 1.0 : kL2KvBudget / out->kv_in_flight_bytes;
-    // HBM: K/V once per head, plus the share of the re-reads that misses L2.
-    const double kv_once = BH * 2.0 * 2.0 * nd;
-    const double kv_streamed = out->l2_bytes - BH * (2.0 * 2.0 * nd + 4.0 * N);
-    out->hbm_bytes = out->io_bytes + (1.0 - out->l2_fit) * (kv_streamed - kv_once);
+    // HBM: K/V once per head.  A head's units run in waves of grid /
+    // heads_in_flight CTAs; the first wave streams the head's K/V in near
+    // lockstep, and each later wave re-reads the share of it that L2 no longer
+    // holds.
+    const double per_head_ctas = static_cast<double>(out->grid) / heads_in_flight;
+    const double waves = per_head_ctas > 0 ? static_cast<double>(pairs) / per_head_ctas : 1.0;
+    const double rereads = waves > 1.0 ? (waves - 1.0) * (1.0 - out->l2_fit) : 0.0;
+    out->hbm_bytes = out->io_bytes + BH * kv_head_bytes * rereads;
     return ATTN_OK;
 }

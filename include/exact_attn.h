@@ -97,8 +97,10 @@ int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, i
  * attn_fwd_host - the same operation on HOST buffers: copies Q, K, V to the
  * device, runs attn_fwd and copies O and LSE back.  The work is split into up
  * to 8 chunks of (batch, head) pairs whose copies in, kernels and copies out
- * run on the library's own per-device streams, so transfers overlap compute;
- * it is ordered after the work already queued on `stream`, and `stream` waits
+ * run on the library's own per-device streams, so transfers overlap compute:
+ * each chunk's kernel starts once its inputs are in, and the copies out start
+ * once every copy in has landed (the two directions share the host link).
+ * It is ordered after the work already queued on `stream`, and `stream` waits
  * for the last copy out.  Pinned host memory makes the copies asynchronous.
  * The caller synchronises `stream` before reading O / LSE.  Calls from several
  * host threads are serialised while they queue their work.
