@@ -69,6 +69,42 @@ def test_backward_negative_and_zero_scale(oracle_mod, scale, causal):
     check(1, 2, 300, 64, causal, 250, oracle_mod, f"scale={scale} causal={causal}", scale=scale)
 
 
+# Whole heads of the benchmarked workloads, in the launch the benchmark times (the full
+# tensors, the workload's seeded recipe, dO drawn with seed + 1000).  The gradients of one
+# (batch, head) depend on that head's inputs alone, so the oracle runs on the listed heads
+# only.  The N = 65536 causal workload is left out: one of its heads costs the fp64 oracle
+# about 1.6e12 multiply-adds.
+WORKLOAD_HEADS = {
+    "b1h1n256d64": [0],
+    "b1h8n4096d64_causal": list(range(8)),
+    "b1h16n16384d128": [0, 15],
+    "b4h32n8192d128_causal_spiky": [0, 127],
+}
+
+
+@pytest.mark.parametrize("name", list(WORKLOAD_HEADS))
+def test_backward_workload_heads(oracle_mod, name):
+    w = workloads.WORKLOADS[name]
+    q, k, v = workloads.workload_inputs(w)
+    do = workloads.make_inputs(w.B, w.H, w.N, w.d, w.seed + 1000)[0]
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = ela.attn_fwd(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = ela.attn_bwd(qd, kd, vd, o, lse, dod, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert ela.last_device_error() == ela.ATTN_OK
+    heads = WORKLOAD_HEADS[name]
+    flat = lambda t: t.reshape(w.B * w.H, w.N, w.d)[heads]
+    ref = oracle_mod.attention_bwd(flat(q), flat(k), flat(v), flat(do), w.causal, w.scale)
+    for gname, g, r in (("dQ", dq, ref[0]), ("dK", dk, ref[1]), ("dV", dv, ref[2])):
+        gg = flat(g.cpu()).double().numpy()
+        for i, h in enumerate(heads):
+            assert np.isfinite(gg[i]).all(), f"{name} head {h} {gname}: non-finite"
+            err = np.abs(gg[i] - r[i]).max()
+            bound = REL * np.abs(r[i]).max() + ABS
+            assert err <= bound, f"{name} head {h} {gname}: max err {err:.3e} > {bound:.3e}"
+            print(f"{name} head {h} {gname}: max err / bound = {err / bound:.3f}")
+
+
 def test_backward_many_heads(oracle_mod):
     check(3, 50, 200, 64, True, 400, oracle_mod, "many heads")
 

@@ -11,13 +11,17 @@ The tensor core takes P and dS rounded to bf16 and accumulates in fp32:
 dV = P^T dO, dK = dS^T Q, dQ = dS K, each written as bf16 at the end. This
 test replays that arithmetic in fp32 and bf16 on the workloads' seeded inputs
 (the spiky recipe among them, whose logits spread far wider than normal
-draws), with O and LSE as the forward writes them (bf16, fp32). It checks the
-result against the oracle under the backward's tolerance reading:
+draws), with O and LSE as the forward kernel forms them (forward_outputs). It
+checks the result against the oracle under the backward's tolerance reading:
     max |g - g_oracle| <= 2e-2 max |g_oracle| + 1e-5   per gradient tensor.
-The margin is recorded too. The modelled error stays below 0.4 of the bound;
-0.15 to 0.30 is observed, at 256 to 4096 positions alike. About half of dQ's
-and dK's error comes from D taken from the bf16 O (a reading: the O the caller
-holds), and most of dV's from the bf16 outputs. P and dS in bf16 add little.
+The margin is printed. Observed: 0.12 to 0.20 of the bound on normal inputs,
+0.13 to 0.62 on the spiky recipe; the assertion keeps the modelled error below
+0.85. dQ and dK take most of theirs from D, computed from the bf16 O the caller
+holds (a reading): on spiky rows that O carries the bf16 rounding of terms the
+forward's stale reference maximum leaves away from 1. Given the GPU forward's
+own O for the spiky workload's last head, this replay gives the GPU backward's
+error there to three digits. Most of dV's error comes from the bf16 outputs.
+P and dS in bf16 add little.
 Planted mistakes (the D term dropped, its sign flipped, the LSE taken
 without the log2 e factor) must break the bound, so the tolerance can tell the
 kernel's arithmetic from a wrong one. The model is not the kernel, whose own
@@ -62,10 +66,32 @@ def backward_replay(q, k, v, o, lse, do, causal, scale, mistake=None):
     return tuple(t.to(torch.bfloat16).double().numpy() for t in (dQ, dK, dV))
 
 
+STALE_LOG2 = 32.0  # the bf16 forward's stale-maximum threshold (log2 units)
+
+
 def forward_outputs(oracle_mod, q, k, v, causal, scale):
-    """O and LSE as the forward writes them: the exact values rounded to bf16 and fp32."""
-    O, L = oracle_mod.attention_rows(q[None], k[None], v[None], causal, scale)
-    return torch.from_numpy(O[0]).to(torch.bfloat16), torch.from_numpy(L[0]).float()
+    """O and LSE as the forward kernel forms them (csrc/attn_fwd_kernel.cuh), in fp32:
+    per row a reference maximum m taken from its first 128-key tile and moved only when a
+    later tile's maximum exceeds it by more than STALE_LOG2; P = 2^(c S - m) rounded to bf16
+    for P V, l summed from the unrounded P, O = (P V) / l rounded to bf16, and
+    LSE = ln 2 (m + log2 l).  With the reference stale, the largest terms of a row are not
+    exactly 1, so their bf16 rounding reaches O, and through D = sum dO O the backward.
+    (oracle_mod is unused: the replay needs no oracle.)"""
+    N = q.shape[0]
+    c = f32(scale) * f32(LOG2E)
+    S = (q.float() @ k.float().T) * c
+    if causal:
+        S = S.masked_fill(torch.arange(N)[None, :] > torch.arange(N)[:, None], -math.inf)
+    pad = (-N) % 128
+    tiles = torch.nn.functional.pad(S, (0, pad), value=-math.inf).reshape(N, -1, 128).max(2).values
+    m = torch.full((N,), -math.inf)
+    for t in range(tiles.shape[1]):
+        m = torch.where(tiles[:, t] > m + STALE_LOG2, tiles[:, t], m)
+    P = torch.exp2(S - m[:, None])
+    l = P.sum(1)
+    O = ((P.to(torch.bfloat16).float() @ v.float()) / l[:, None]).to(torch.bfloat16)
+    lse = ((m + torch.log2(l)) * f32(math.log(2.0))).float()
+    return O, lse
 
 
 def head(name, b, h, n):
@@ -81,6 +107,7 @@ CASES = [  # workload, (b, h), leading positions taken
     ("b1h16n16384d128", (0, 5), 1024),
     ("b4h32n8192d128_causal_spiky", (1, 9), 2048),
     ("b4h32n8192d128_causal_spiky", (3, 30), 1024),
+    ("b4h32n8192d128_causal_spiky", (3, 31), 4096),  # dQ's worst row on the GPU (3733) lies here
 ]
 
 
@@ -105,7 +132,8 @@ def test_backward_arithmetic_meets_the_tolerance_with_margin(cases, name, bh, n)
     w, q, k, v, do, o, lse, ref = cases[(name, *bh)]
     got = backward_replay(q, k, v, o, lse, do, w.causal, w.scale)
     r = ratios(got, ref)
-    assert max(r) <= 0.4, dict(zip(("dQ", "dK", "dV"), r))
+    print(name, bh, n, dict(zip(("dQ", "dK", "dV"), (round(x, 3) for x in r))))
+    assert max(r) <= 0.85, dict(zip(("dQ", "dK", "dV"), r))
 
 
 @pytest.mark.parametrize("mistake", ["no_D", "D_sign", "lse_natural"])
