@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import exact_long_sequence_gb300 as ela
+from exact_long_sequence_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
 
@@ -82,6 +83,29 @@ def test_layernorm_constant_rows_give_beta_and_in_place(oracle_mod):
     xd = x.cuda()
     ela.layernorm_rows(xd, g.cuda(), b.cuda(), eps=1e-3, out=xd)
     torch.testing.assert_close(xd.cpu(), b.expand(3, N), rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("name", list(workloads.ROW_WORKLOADS))
+def test_row_workloads_sampled(oracle_mod, name):
+    """The benchmarked row workloads at full size, on the benchmark's seeded host inputs and in
+    its call (the softmax with the workspace its segmented path asks for): 64 sampled rows
+    against the oracle, and every row's softmax sum."""
+    kind, R, N = workloads.ROW_WORKLOADS[name]
+    inp = workloads.row_inputs(kind, R, N, seed=1)
+    rows_idx = torch.sort(torch.randperm(R, generator=torch.Generator().manual_seed(7))[:64]).values
+    if kind == "softmax":
+        need = ela.load_library().attn_softmax_rows_workspace_bytes(R, N)
+        ws = torch.empty(max(need, 8), dtype=torch.uint8, device="cuda") if need else None
+        y = ela.softmax_rows(inp.cuda(), workspace=ws)
+        torch.cuda.synchronize()
+        sums = y.float().sum(-1)
+        assert (sums - 1).abs().max().item() <= 2.0 ** -7
+        check_softmax(oracle_mod, inp[rows_idx], y[rows_idx.cuda()])
+    else:
+        x, g, b = inp
+        y = ela.layernorm_rows(x.cuda(), g.cuda(), b.cuda(), eps=1e-5)
+        torch.cuda.synchronize()
+        check_layernorm(oracle_mod, x[rows_idx], g, b, 1e-5, y[rows_idx.cuda()])
 
 
 def test_row_ops_reject_bad_shapes():
