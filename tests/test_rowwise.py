@@ -75,6 +75,17 @@ def test_layernorm_rows_parity(oracle_mod, R, N):
     check_layernorm(oracle_mod, x, g, b, 1e-5, y)
 
 
+@pytest.mark.parametrize("R,N", [(2000, 8), (3001, 1000), (1000, 2048), (700, 11264), (700, 11272)])
+def test_layernorm_many_rows_parity(oracle_mod, R, N):
+    """Many rows (several waves of one CTA per row), rows of one to 1409 chunks."""
+    x = rows(R, N, seed=N + 3 * R, scale=1.0, offset=3.0)
+    gen = torch.Generator().manual_seed(N + 1)
+    g = (1 + 0.2 * torch.randn(N, generator=gen)).to(torch.bfloat16)
+    b = (0.3 * torch.randn(N, generator=gen)).to(torch.bfloat16)
+    y = ela.layernorm_rows(x.cuda(), g.cuda(), b.cuda(), eps=1e-5)
+    check_layernorm(oracle_mod, x, g, b, 1e-5, y)
+
+
 def test_layernorm_constant_rows_give_beta_and_in_place(oracle_mod):
     N = 512
     x = torch.full((3, N), -2.5, dtype=torch.bfloat16)
