@@ -77,6 +77,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=None, help="named workload (default: the long-sequence headline case)")
     ap.add_argument("--skip-e2e", action="store_true", help="omit the host-buffer end-to-end leg")
     ap.add_argument("--skip-cpu", action="store_true", help="omit the CPU-oracle baseline leg")
+    ap.add_argument("--keep-l2", action="store_true",
+                    help="no L2 flush between steps: back-to-back launches whose DRAM counters (ncu, cache control "
+                         "off) give a step's steady-state traffic; not a timing configuration")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-baseline sample")
     ap.add_argument("--fp8", action="store_true", help="time the FP8 (E4M3) forward instead of the bf16 one")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "softmax", "layernorm"], default="fwd",
@@ -264,6 +267,12 @@ def run_reference(args, w):
     return 0
 
 
+def l2_note(args) -> str:
+    if args.keep_l2:
+        return "kept between steps (back-to-back launches for DRAM counter captures; not a timing configuration)"
+    return f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"
+
+
 def workload_config(w, l2_note):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
             "scale": w.scale, "inputs": f"seeded synthetic ({w.qk_dist} Q,K; {w.v_dist} V), bf16",
@@ -369,7 +378,8 @@ def run_gb300_fp8(args, w):
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
-            flush.zero_()
+            if not args.keep_l2:
+                flush.zero_()
             starts[i].record(stream)
             ela.attn_fwd_fp8(q8, k8, v8, scales, causal=w.causal, scale=w.scale, out=o, lse=lse, workspace=ws,
                              stream=stream)
@@ -406,7 +416,7 @@ def run_gb300_fp8(args, w):
         "metric": METRIC + " (FP8 E4M3 inputs)", "precision": "e4m3", "value": value, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": slowest * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": workload_config(w, f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"),
+        "config": workload_config(w, l2_note(args)),
         "roofline": roofline, "gpu_launches": fp8_launches * args.steps, "clocks": clocks.summary(),
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
         "e2e": None,
@@ -507,7 +517,8 @@ def run_gb300_rows(args, kind):
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
-            flush.zero_()
+            if not args.keep_l2:
+                flush.zero_()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
@@ -531,7 +542,7 @@ def run_gb300_rows(args, kind):
         "warmup": args.warmup, "ms_per_step": slowest * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": name, "R": R, "N": N, "inputs": "seeded synthetic normal rows, bf16",
-                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)",
+                   "l2": l2_note(args),
                    "parallelism": "replicas", "reads_of_x_per_step": passes},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json)",
@@ -591,7 +602,8 @@ def run_gb300_bwd(args, w):
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
-            flush.zero_()
+            if not args.keep_l2:
+                flush.zero_()
             starts[i].record(stream)
             ela.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, workspace=ws, stream=stream)
             ends[i].record(stream)
@@ -624,7 +636,7 @@ def run_gb300_bwd(args, w):
         "metric": METRIC_BWD, "pass": "bwd", "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": slowest * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"),
+        "config": workload_config(w, l2_note(args)),
         "roofline": roofline, "gpu_launches": 3 * args.steps, "clocks": clocks.summary(),
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
         "e2e": None,
@@ -689,7 +701,8 @@ def run_gb300(args, w):
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
-            flush.zero_()
+            if not args.keep_l2:
+                flush.zero_()
             starts[i].record(stream)
             ela.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream, workspace=split_ws)
             ends[i].record(stream)
@@ -720,7 +733,8 @@ def run_gb300(args, w):
             dist.barrier()
         e_ms = []
         for _ in range(max(3, args.steps // 2)):
-            flush.zero_()
+            if not args.keep_l2:
+                flush.zero_()
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
             ela.attn_fwd_host(qh, kh, vh, causal=w.causal, scale=w.scale, out_h=oh, lse_h=lh, workspace=ws,
@@ -756,7 +770,7 @@ def run_gb300(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"),
+        "config": workload_config(w, l2_note(args)),
         "roofline": roofline,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
