@@ -79,7 +79,7 @@ int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, con
         // attention kernel's retire, and wait in-kernel for its completion
         const int rows = p.split_units * 2 * kBr;  // the rows of the split units
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+        cfg.gridDim = dim3(static_cast<unsigned>((rows + kCombineRowsPerCta - 1) / kCombineRowsPerCta));
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
@@ -88,7 +88,9 @@ int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, con
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if ((e = cudaLaunchKernelEx(&cfg, attn_fwd_combine_kernel<D, CAUSAL>, p)) != cudaSuccess) return cuda_fail(e);
+        auto combine = p.kv_split == 2 ? attn_fwd_combine_kernel<D, CAUSAL, 2>
+                       : p.kv_split == 3 ? attn_fwd_combine_kernel<D, CAUSAL, 3> : attn_fwd_combine_kernel<D, CAUSAL, 4>;
+        if ((e = cudaLaunchKernelEx(&cfg, combine, p)) != cudaSuccess) return cuda_fail(e);
     }
     return ATTN_OK;
 }

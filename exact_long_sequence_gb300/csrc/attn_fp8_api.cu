@@ -86,7 +86,7 @@ int launch_fp8(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq,
         // the segments' merge, as a programmatic dependent launch (see attn_api.cu)
         const int rows = p.split_units * 2 * kBr;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+        cfg.gridDim = dim3(static_cast<unsigned>((rows + kCombineRowsPerCta - 1) / kCombineRowsPerCta));
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
@@ -95,7 +95,9 @@ int launch_fp8(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq,
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if ((e = cudaLaunchKernelEx(&cfg, attn_fwd_combine_kernel<kFp8D, CAUSAL>, p)) != cudaSuccess) return cuda_fail(e);
+        auto combine = p.kv_split == 2 ? attn_fwd_combine_kernel<kFp8D, CAUSAL, 2>
+                       : p.kv_split == 3 ? attn_fwd_combine_kernel<kFp8D, CAUSAL, 3> : attn_fwd_combine_kernel<kFp8D, CAUSAL, 4>;
+        if ((e = cudaLaunchKernelEx(&cfg, combine, p)) != cudaSuccess) return cuda_fail(e);
     }
     return ATTN_OK;
 }

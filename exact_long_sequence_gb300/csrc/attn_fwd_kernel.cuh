@@ -709,14 +709,36 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 // results (O_s = softmax over the segment's keys times V, LSE_s),
 //     LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s,
 // the same online-softmax combination as inside the kernel, across segments,
-// in the fixed segment order.  One warp per row of the split units (2 kBr rows
-// each; lane l holds columns [kPer l, kPer l + kPer), so every partial row is
-// one coalesced read); the rows of the other units were written by the
-// attention kernel itself.  After the merged row is written, its partial O
-// lines are discarded from L2: nothing reads them again, so they are not
-// written back to device memory.
-template <int D, bool CAUSAL>
+// in the fixed segment order.  SEG is the launch's segment count, so that a
+// thread holds only the partials that exist (its registers set how many CTAs
+// an SM holds at once).  One warp per row of the split units (2 kBr rows
+// each); lane l holds columns [kPer l, kPer l + kPer) of the row, one vector
+// load per segment, so every partial row is one coalesced read.  The rows of
+// the other units were written by the attention kernel itself.  After the
+// merged row is written, its partial O lines are discarded from L2: nothing
+// reads them again, so they are not written back to device memory.
+constexpr int kCombineRowsPerCta = 8;  // 256 threads, one warp per row
+
+template <int D>
+struct CombineVec;  // one lane's kPer = D / 32 fp32 columns of a partial row
+template <>
+struct CombineVec<64> {
+    __device__ static void load(const float* src, float (&x)[2]) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+        x[0] = v.x, x[1] = v.y;
+    }
+};
+template <>
+struct CombineVec<128> {
+    __device__ static void load(const float* src, float (&x)[4]) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+        x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+    }
+};
+
+template <int D, bool CAUSAL, int SEG>
 __global__ void __launch_bounds__(256) attn_fwd_combine_kernel(const FwdParams p) {
+    static_assert(SEG >= 2 && SEG <= kMaxKvSplit, "segments");
     constexpr int kPer = D / 32;                 // columns per lane
     constexpr int kLinesPerRow = D * 4 / 128;   // 128-byte lines of one partial row
     // launched as a programmatic dependent of the attention kernel: wait until
@@ -731,23 +753,21 @@ __global__ void __launch_bounds__(256) attn_fwd_combine_kernel(const FwdParams p
     const int qrow = ui.q0 * kBr + rr;
     if (qrow >= p.N) return;
     const size_t row = static_cast<size_t>(ui.bh) * p.N + qrow;
-    const int nseg = p.kv_split;
-    const size_t base = static_cast<size_t>(ord) * nseg * (2 * kBr) + rr;  // segment s at base + s * 2 kBr
-    float w[kMaxKvSplit];
-    float x[kMaxKvSplit][kPer];
-    float mx = -INFINITY;
+    const size_t base = static_cast<size_t>(ord) * SEG * (2 * kBr) + rr;  // segment s at base + s * 2 kBr
+    float w[SEG];
+    float x[SEG][kPer];
 #pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) {
-        w[s] = s < nseg ? __ldcg(p.part_lse + base + s * (2 * kBr)) : -INFINITY;
-        mx = fmaxf(mx, w[s]);
-        const float* src = p.part_o + (base + s * (2 * kBr)) * D + lane * kPer;
-#pragma unroll
-        for (int c = 0; c < kPer; ++c) x[s][c] = s < nseg ? __ldcg(src + c) : 0.f;
+    for (int s = 0; s < SEG; ++s) {
+        w[s] = __ldcg(p.part_lse + base + s * (2 * kBr));
+        CombineVec<D>::load(p.part_o + (base + s * (2 * kBr)) * D + lane * kPer, x[s]);
     }
+    float mx = w[0];
+#pragma unroll
+    for (int s = 1; s < SEG; ++s) mx = fmaxf(mx, w[s]);
     float wsum = 0.f;
 #pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) {
-        w[s] = s < nseg ? expf(w[s] - mx) : 0.f;  // now the segment weights
+    for (int s = 0; s < SEG; ++s) {
+        w[s] = expf(w[s] - mx);  // now the segment weights
         wsum += w[s];
     }
     const float inv = 1.f / wsum;
@@ -755,7 +775,7 @@ __global__ void __launch_bounds__(256) attn_fwd_combine_kernel(const FwdParams p
 #pragma unroll
     for (int c = 0; c < kPer; ++c) acc[c] = 0.f;
 #pragma unroll
-    for (int s = 0; s < kMaxKvSplit; ++s) {
+    for (int s = 0; s < SEG; ++s) {
         const float ws = w[s] * inv;
 #pragma unroll
         for (int c = 0; c < kPer; ++c) acc[c] = fmaf(ws, x[s][c], acc[c]);
@@ -765,7 +785,7 @@ __global__ void __launch_bounds__(256) attn_fwd_combine_kernel(const FwdParams p
     for (int c = 0; c < kPer; c += 2) dst[c / 2] = pack_bf16x2(acc[c], acc[c + 1]);
     if (lane == 0) p.LSE[row] = mx + logf(wsum);
     // every value read above has been consumed by the stores: drop the lines
-    if (lane < nseg * kLinesPerRow) {
+    if (lane < SEG * kLinesPerRow) {
         const int s = lane / kLinesPerRow, part = lane - s * kLinesPerRow;
         l2_discard_line(reinterpret_cast<const char*>(p.part_o + (base + s * (2 * kBr)) * D) + part * 128);
     }
