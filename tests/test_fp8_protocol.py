@@ -12,9 +12,11 @@ k + 2 as phase k.  The protocol must never let a barrier run two phases ahead
 of a waiter, and must never deadlock.
 
 This test replays every wait and arrival of the five roles, with the same counts
-and the same unit schedule as the kernel, under many random interleavings.  It
+and the same work items as the kernel, under many random interleavings.  It
 checks both properties over causal and non-causal schedules, several units per
-CTA, and an odd number of query tiles.  Where a role's arrival completes an
+CTA, an odd number of query tiles, and the K/V segments [jb, je) of split units
+(alone and followed by whole units), where every item loads its own Q tiles and
+its first product (jj == jb) starts O after the previous item's O was read out.  Where a role's arrival completes an
 asynchronous operation (a TMA load, an MMA commit), the model completes it at
 once; that is the most permissive timing for run-ahead.  A negative control
 shows the check finds the race of a protocol with one P barrier per tile, which
@@ -55,7 +57,28 @@ def unit_tiles(u, nq, BH, causal, heads_per_group):
     return [min(q0 + t + 1, nq) if causal else nq for t in (0, 1)]
 
 
-def run(units, nq, BH, causal, G, seed, per_buffer_p=True, dynamic=False):
+def unit_items(units, nq, BH, causal, G):
+    """Whole units as work items (jb, je, n0): tile 0 visits [jb, min(je, n0)), tile 1 [jb, je)."""
+    out = []
+    for u in units:
+        n = unit_tiles(u, nq, BH, causal, G)
+        out.append((0, n[1], n[0]))
+    return out
+
+
+def split_items(units, nq, BH, causal, G, nseg):
+    """Every unit cut into nseg K/V segments of ceil(n1 / nseg) tiles (the kernel's decode_item)."""
+    out = []
+    for u in units:
+        n = unit_tiles(u, nq, BH, causal, G)
+        c = -(-n[1] // nseg)
+        for sgi in range(nseg):
+            jb = sgi * c
+            out.append((jb, min(n[1], jb + c), n[0]))
+    return out
+
+
+def run(items, seed, per_buffer_p=True, dynamic=False):
     """Returns None, or a description of a deadlock or of a phase overrun."""
     rng = random.Random(seed)
     B = {}
@@ -89,13 +112,12 @@ def run(units, nq, BH, causal, G, seed, per_buffer_p=True, dynamic=False):
 
     def producer():
         pos = 0
-        for ul, u in enumerate(units):
-            n = unit_tiles(u, nq, BH, causal, G)
+        for ul, (jb, je, _) in enumerate(items):
             for t in (0, 1):
                 if ul:
                     yield wait(("QEmpty", t), ul - 1)
                 B[("QFull", t)].arrive()
-            for _ in range(2 * n[1]):  # K_j, V_j for every tile of the unit
+            for _ in range(2 * (je - jb)):  # K_j, V_j for every tile of the item
                 st, use = pos % STAGES, pos // STAGES
                 if use:
                     yield wait(("KvEmpty", st), use - 1)
@@ -108,12 +130,11 @@ def run(units, nq, BH, causal, G, seed, per_buffer_p=True, dynamic=False):
 
     def mma(t):
         s_cnt = p_cnt = kpos = 0
-        for ul, u in enumerate(units):
-            n = unit_tiles(u, nq, BH, causal, G)
-            n1, nt = n[1], n[t]
+        for ul, (jb, n1, n0) in enumerate(items):
+            nt = min(n1, n0) if t == 0 else n1  # this tile's K/V tiles are [jb, nt)
             yield wait(("QFull", t), ul)
             kp, vp = kpos, kpos + 1
-            for j in range(n1 + 1):
+            for j in range(jb, n1 + 1):
                 if j < n1:
                     yield wait(("KvFull", kp % STAGES), kp // STAGES)
                     if j < nt:
@@ -125,13 +146,13 @@ def run(units, nq, BH, causal, G, seed, per_buffer_p=True, dynamic=False):
                         s_cnt += 1
                     B[("KvEmpty", kp % STAGES)].arrive()
                     kp += 2
-                if j == 0:
+                if j == jb:
                     continue
                 jj = j - 1
                 yield wait(("KvFull", vp % STAGES), vp // STAGES)
                 if jj < nt:
                     yield wait(*pbar("PHalf", t, p_cnt))
-                    if jj == 0 and ul:
+                    if jj == jb and ul:
                         yield wait(("OEmpty", t), ul - 1)
                     yield wait(*pbar("PFull", t, p_cnt))
                     B[("PFree", t, p_cnt & 1)].arrive()
@@ -148,14 +169,14 @@ def run(units, nq, BH, causal, G, seed, per_buffer_p=True, dynamic=False):
 
     def softmax(t):
         s = 0
-        for ul, u in enumerate(units):
-            n = unit_tiles(u, nq, BH, causal, G)
-            for j in range(n[t]):
+        for ul, (jb, je, n0) in enumerate(items):
+            nt = min(je, n0) if t == 0 else je
+            for j in range(jb, nt):
                 yield wait(("SFull", t), s)
                 if s >= 2:
                     yield wait(("PFree", t, s & 1), (s >> 1) - 1)
                 B[("SCons", t)].arrive(128)
-                if j > 0 and rng.random() < 0.3:  # a row's maximum moved: rescale O
+                if j > jb and rng.random() < 0.3:  # a row's maximum moved: rescale O
                     yield wait(("ODone", t), s - 1)
                 B[pbar("PHalf", t, s)[0]].arrive(128)
                 B[pbar("PFull", t, s)[0]].arrive(128)
@@ -207,17 +228,40 @@ def test_protocol_has_no_overrun_and_no_deadlock(nq, BH, causal, grid, G, dynami
     for block in range(0, min(grid, units), 5):
         mine = list(range(block, units, grid))[:3]
         for seed in range(12):
-            assert run(mine, nq, BH, causal, G, seed, dynamic=dynamic) is None
+            assert run(unit_items(mine, nq, BH, causal, G), seed, dynamic=dynamic) is None
 
 
 def test_dynamic_schedule_with_a_claimed_unit_order():
     """Units claimed out of stride order (as the counter hands them out), causal."""
     for mine in ([0, 7, 9, 30, 31], [3, 4, 5], [60, 2, 13]):
         for seed in range(20):
-            assert run(mine, 64, 8, True, 8, seed, dynamic=True) is None
+            assert run(unit_items(mine, 64, 8, True, 8), seed, dynamic=True) is None
+
+
+SPLIT_CASES = [  # (query tiles per head, batch x heads, causal, heads per group, segments, the CTA's units)
+    (64, 8, True, 8, 2, [0, 1, 2]),       # the heaviest causal units, two segments each
+    (64, 8, True, 8, 4, [0, 8]),          # four segments (each still holds a tile of query tile 0)
+    (32, 1, False, 1, 3, [13, 14, 15]),   # the last units of a non-causal launch, three segments
+    (33, 3, True, 3, 2, [0, 3, 6]),       # odd query-tile count
+]
+
+
+@pytest.mark.parametrize("dynamic", [False, True])
+@pytest.mark.parametrize("nq,BH,causal,G,nseg,mine", SPLIT_CASES)
+def test_protocol_with_kv_segments(nq, BH, causal, G, nseg, mine, dynamic):
+    """The split instantiation: items are K/V segments [jb, je) of units; every item loads
+    its own Q tiles, and its first product starts O afresh (jj == jb)."""
+    items = split_items(mine, nq, BH, causal, G, nseg)
+    for jb, je, n0 in items:  # the split rule: every segment holds a tile of each query tile
+        assert jb < min(je, n0)
+    # segments, then whole units, as a CTA meets them when only some units are split
+    mixed = items + unit_items([mine[-1] + 1], nq, BH, causal, G)
+    for seed in range(15):
+        assert run(items, seed, dynamic=dynamic) is None
+        assert run(mixed, seed, dynamic=dynamic) is None
 
 
 def test_checker_finds_the_single_p_barrier_race():
     units = list(range(0, 256, 152))
-    found = [run(units, 64, 8, True, 8, seed, per_buffer_p=False) for seed in range(12)]
+    found = [run(unit_items(units, 64, 8, True, 8), seed, per_buffer_p=False) for seed in range(12)]
     assert any(f and f.startswith("phase overrun") for f in found)
