@@ -399,7 +399,10 @@ def run_gb300_fp8(args, w):
     peak_bf16, peak_bf16_sustained, peak_kind = read_peaks()
     peak = 2.0 * peak_bf16
     # the V transpose and the attention kernel, plus the combine kernel of a K/V split
-    fp8_launches = 3 if ela.split_segments(w.B, w.H, w.N, w.d, w.causal) > 1 else 2
+    # the V transpose and the attention kernel, plus the counter-zeroing kernel of the dynamic
+    # schedule and the combine kernel of a K/V split
+    choice = ela.split_choice(w.B, w.H, w.N, w.d, w.causal)
+    fp8_launches = 2 + int(choice["dynamic"]) + int(choice["segs"] > 1)
     kernel_ms = statistics.mean(step_ms)
     achieved = w.flops / (kernel_ms / 1e3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
@@ -682,11 +685,15 @@ def run_gb300(args, w):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     # Workloads with fewer work units than SMs, or a partial last wave, take the K/V split (the
     # attention kernel and the combine kernel); causal workloads take the dynamic schedule (a
-    # counter zeroed by a 4-byte memset on the stream before each launch).  The workspace is
+    # counter zeroed by a one-thread kernel on the stream before each launch).  The workspace is
     # allocated once, outside the timed region.
     split_bytes = ela.split_workspace_bytes(w.B, w.H, w.N, w.d, w.causal)
     split_ws = torch.empty(split_bytes, dtype=torch.uint8, device=dev) if split_bytes else None
-    launches_per_step = 2 if ela.split_segments(w.B, w.H, w.N, w.d, w.causal) > 1 else 1
+    choice = ela.split_choice(w.B, w.H, w.N, w.d, w.causal)
+    split_step = choice["segs"] > 1
+    # the attention kernel, plus the counter-zeroing kernel of the dynamic schedule and the
+    # combine kernel of a K/V split
+    launches_per_step = 1 + int(choice["dynamic"]) + int(split_step)
 
     for _ in range(max(3, args.warmup)):
         ela.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream, workspace=split_ws)
@@ -761,7 +768,7 @@ def run_gb300(args, w):
                 "traffic": recorded_traffic(w.name),
                 "algorithmic_flops_per_launch": w.flops, "kernel_ms": kernel_ms,
                 "io_bound_bytes": w.io_bytes}
-    if launches_per_step == 2:
+    if split_step:
         roofline["note"] = ("K/V split: the step is the attention kernel plus the combine kernel (about 1 % of "
                             "it); the step time is used for both")
     if peak_sustained:

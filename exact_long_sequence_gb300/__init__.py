@@ -171,6 +171,24 @@ def split_workspace_bytes(B: int, H: int, N: int, d: int, causal: bool) -> int:
     return int(load_library().attn_fwd_split_workspace_bytes(B, H, N, d, int(bool(causal))))
 
 
+def split_choice(B: int, H: int, N: int, d: int, causal: bool, num_sms: int | None = None) -> dict:
+    """The work split attn_fwd_split uses (host only): segments per split unit (1: none), the
+    first split unit, the number of split units, and whether the dynamic schedule runs (a
+    counter-zeroing kernel then precedes the attention kernel).  num_sms: the current device's
+    by default."""
+    import ctypes
+
+    import torch
+
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    out = [ctypes.c_int(0) for _ in range(4)]
+    st = load_library().attn_fwd_split_choice(B, H, N, d, int(bool(causal)), int(num_sms),
+                                              *[ctypes.byref(x) for x in out])
+    _check(st, "attn_fwd_split_choice")
+    return {"segs": out[0].value, "first": out[1].value, "units": out[2].value, "dynamic": bool(out[3].value)}
+
+
 def split_segments(B: int, H: int, N: int, d: int, causal: bool) -> int:
     """K/V segments per split unit attn_fwd_split chooses (1: no split; 0: invalid or no device)."""
     return int(load_library().attn_fwd_split_segments(B, H, N, d, int(bool(causal))))

@@ -71,9 +71,24 @@ int launch(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq, con
     }
     // every CTA starts with item blockIdx.x: the grid never exceeds the items
     const int grid = p.num_items < dev.num_sms ? p.num_items : dev.num_sms;
-    kernel<<<grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e);
+    cudaError_t e;
+    if constexpr (DYN) {
+        // a programmatic dependent of the counter's zeroing kernel (see there)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(static_cast<unsigned>(plan.threads));
+        cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, p)) != cudaSuccess) return cuda_fail(e);
+    } else {
+        kernel<<<grid, plan.threads, plan.smem_bytes, stream>>>(tq, tk, tv, p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    }
     if (p.kv_split > 1) {
         // programmatic dependent launch: the combine kernel's CTAs may start as the
         // attention kernel's retire, and wait in-kernel for its completion
@@ -146,7 +161,8 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
     p.part_lse = kv_split > 1 ? reinterpret_cast<float*>(ws + kCounterBlock + split_part_o_bytes(split, d)) : nullptr;
     p.sched_counter = dynamic ? reinterpret_cast<int*>(ws) : nullptr;
     if (dynamic) {
-        cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), stream);
+        zero_sched_counter_kernel<<<1, 1, 0, stream>>>(reinterpret_cast<int*>(ws));
+        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e);
     }
     take_armed_hook(p);

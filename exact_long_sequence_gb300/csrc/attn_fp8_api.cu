@@ -80,8 +80,23 @@ int launch_fp8(DeviceState& dev, const attn_plan_t& plan, const CUtensorMap& tq,
     }
     // every CTA starts with item blockIdx.x: the grid never exceeds the items
     const int grid = p.num_items < dev.num_sms ? p.num_items : dev.num_sms;
-    kernel<<<grid, plan.threads, smem, stream>>>(tq, tk, tvt, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    if constexpr (DYN) {
+        // a programmatic dependent of the counter's zeroing kernel
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(static_cast<unsigned>(plan.threads));
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, kernel, tq, tk, tvt, p)) != cudaSuccess) return cuda_fail(e);
+    } else {
+        kernel<<<grid, plan.threads, smem, stream>>>(tq, tk, tvt, p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    }
     if (p.kv_split > 1) {
         // the segments' merge, as a programmatic dependent launch (see attn_api.cu)
         const int rows = p.split_units * 2 * kBr;
@@ -203,9 +218,11 @@ extern "C" int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void
         split.segs > 1 ? reinterpret_cast<float*>(counter_block + kCounterBlock + split_part_o_bytes(split, d)) : nullptr;
     p.sched_counter = nullptr;
     if (split.dynamic) {
-        // CTAs claim items, heaviest first, from a counter zeroed on the stream
+        // CTAs claim items, heaviest first, from a counter zeroed on the stream by a
+        // kernel the attention launch depends on programmatically (see attn_api.cu)
         int* counter = reinterpret_cast<int*>(counter_block);
-        cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
+        zero_sched_counter_kernel<<<1, 1, 0, stream>>>(counter);
+        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e);
         p.sched_counter = counter;
     }

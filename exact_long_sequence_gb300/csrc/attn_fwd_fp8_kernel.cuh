@@ -240,6 +240,8 @@ attn_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_con
             if (!ok) break;
             if constexpr (DYN) {
                 // claim this CTA's next item and publish it to the other roles
+                // the counter was zeroed by the grid this one depends on: wait for it first
+                if (r == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 w = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
                 if (w >= p.num_items) w = -1;
                 const uint32_t s = r % kItemRing;

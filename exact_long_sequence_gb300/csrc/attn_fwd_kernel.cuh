@@ -362,6 +362,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             ++ul;
             if constexpr (DYN) {
                 // claim this CTA's next item and publish it to the other roles
+                // the counter was zeroed by the grid this one depends on (see
+                // zero_sched_counter_kernel): wait for it before the first claim
+                if (r == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 w = static_cast<int>(gridDim.x) + atomicAdd(p.sched_counter, 1);
                 if (w >= p.num_items) w = -1;
                 const uint32_t s = r % kItemRing;
@@ -703,6 +706,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Zeroes the dynamic schedule's claim counter ahead of an attention launch that
+// depends on it programmatically: that launch's CTAs start at once (each first
+// runs item blockIdx.x) and its producer waits for this grid only before its
+// first claim, so the zeroing overlaps the attention kernel's start.
+static __global__ void zero_sched_counter_kernel(int* counter) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    *counter = 0;
 }
 
 // Merge the segments of the split units: per row, with the segments' partial

@@ -138,8 +138,10 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int N, int d);
  * the IO-Aware Algorithms page) applied across segments, then drops the
  * partial rows from L2 without writing them back.  The result is the same
  * operation as attn_fwd, up to floating-point rounding.  Launches on `stream`:
- * a 4-byte memset of the schedule counter (dynamic schedule only), the
- * attention kernel, and the combine kernel (split launches only).
+ * a one-thread kernel that zeroes the schedule counter (dynamic schedule only;
+ * the attention kernel is its programmatic dependent and waits for it only
+ * before its first claim), the attention kernel, and the combine kernel (split
+ * launches only).
  *   arguments as attn_fwd, plus
  *   workspace       : device buffer of at least attn_fwd_split_workspace_bytes()
  *                     bytes, 16-byte aligned, owned by the caller, not used by
@@ -304,10 +306,11 @@ int attn_noalloc_last_device_error(cudaStream_t stream);
  *                aligned, owned by the caller, not used by other work while this
  *                call runs: V transposed to [B,H,d,N] (rows padded to 16 bytes),
  *                then the schedule counter, written by this call
- * d must be 128 (ATTN_ERR_UNSUPPORTED otherwise).  Two launches on `stream`
- * (the transpose of V, then the attention kernel; a 4-byte memset before the
- * latter under the dynamic schedule); the same argument, size and error rules
- * as attn_fwd otherwise.
+ * d must be 128 (ATTN_ERR_UNSUPPORTED otherwise).  Launches on `stream`: the
+ * transpose of V, then the attention kernel; under the dynamic schedule a
+ * one-thread kernel zeroing the schedule counter comes between them, and a
+ * split launch ends with the combine kernel.  The same argument, size and error
+ * rules as attn_fwd otherwise.
  */
 int attn_fwd_fp8(const void* Q8, const void* K8, const void* V8, void* O, float* LSE, int B, int H, int N, int d,
                  int causal, float scale, float q_scale, float k_scale, float v_scale, void* workspace,
